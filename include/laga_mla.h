@@ -1,0 +1,167 @@
+/*
+ * laga_mla.h — C ABI of the LAGA MLA attention block for one GPU (sm_103a).
+ *
+ * What the operation is
+ * ---------------------
+ * "A Training-Memory Regression in MLA Sequence Parallelism: Why Megatron-Core
+ * Forbids Absorption, and LAGA -- a Communication-Efficient Fix" (weekinpapers
+ * page, Abstract): LAGA keeps the absorbed MLA form's communication -- only the
+ * compressed latent is all-gathered across the sequence-parallel (SP) group --
+ * but rejects the absorb reformulation and instead rebuilds every head's K and
+ * V locally from the gathered latent, then runs ordinary (explicit-form)
+ * attention. The Abstract states the result is bit-identical to the explicit
+ * form at SP=1. This library is that local computation on one SP rank. The
+ * all-gather itself is outside it: the gathered latent is an input.
+ *
+ * For each batch element b, head h, local query i (absolute position
+ * q_offset + i) and latent row j:
+ *   K_nope[j,h,:] = c_kv[j,:] . W_UK[:, h*d_nope : (h+1)*d_nope]     (rebuild K)
+ *   V[j,h,:]      = c_kv[j,:] . W_UV[:, h*d_v    : (h+1)*d_v]        (rebuild V)
+ *   K_h[j]        = [K_nope[j,h,:] | k_rope[j,:]]     (one RoPE key shared by all heads)
+ *   s_ij          = softmax_scale * q[i,h,:] . K_h[j], visible iff j <= q_offset+i
+ *                   (causal) or always (non-causal)
+ *   lse[h,i]      = ln sum_j exp(s_ij)                 over visible j
+ *   out[i,h,:]    = sum_j exp(s_ij - lse[h,i]) V[j,h,:]
+ * and the backward of the loss <dout, out> with respect to q, c_kv, k_rope,
+ * W_UK and W_UV.
+ *
+ * Layouts (dense, row-major, innermost last)
+ * ------------------------------------------
+ *   q       [B, Sq, n_h, d_nope + d_rope]  no-RoPE part first, then RoPE part
+ *   c_kv    [B, Skv, d_c]                  the gathered latent
+ *   k_rope  [B, Skv, d_rope]               already rotated
+ *   W_UK    [d_c, n_h * d_nope]            column h*d_nope + k belongs to head h
+ *   W_UV    [d_c, n_h * d_v]               column h*d_v + k belongs to head h
+ *   out     [B, Sq, n_h, d_v]
+ *   lse     [B, n_h, Sq]                   always fp32, natural log of scaled scores
+ *   dq, dc_kv, dk_rope, dW_UK, dW_UV       the shapes of q, c_kv, k_rope, W_UK, W_UV
+ *
+ * Conventions
+ * -----------
+ *  - Element type: every tensor has desc->dtype except lse (always fp32).
+ *  - Ownership: the caller allocates every buffer, outputs and workspace
+ *    included. The library allocates, frees and synchronises nothing
+ *    (laga_mla_check excepted, which synchronises the given stream). All work
+ *    is enqueued on the given stream (a cudaStream_t; NULL = legacy default).
+ *  - Outputs are overwritten, never accumulated into.
+ *  - Latent rows no query of the shard can see (j >= q_offset + Sq when causal)
+ *    get zero dc_kv and dk_rope.
+ *  - Alignment: every pointer 16-byte aligned. Otherwise LAGA_ERR_INVALID_ARG.
+ *  - Errors: argument errors are found on the host and returned before any
+ *    launch. Launch failures return LAGA_ERR_CUDA. A device-side wait that runs
+ *    out (a bounded mbarrier wait) records LAGA_ERR_TIMEOUT in a per-device
+ *    status word that laga_mla_check reads. No call aborts the process.
+ *  - Threads: calls are re-entrant as long as concurrent calls use disjoint
+ *    workspaces and outputs.
+ *  - Reproducibility: the backward adds per-key-tile contributions to dq with
+ *    fp32 atomics, so dq may differ in the last bits between runs; every other
+ *    output is produced in a fixed order.
+ *
+ * Supported problems
+ * ------------------
+ *  - dtype BF16 with d_c = 512, d_nope = d_v = 128, d_rope = 64 (the
+ *    DeepSeek-V3 dimensions): tensor-core path (tcgen05/TMEM/TMA).
+ *  - dtype F32, any dims with d_nope + d_rope <= 256, d_v <= 256, d_c <= 1024:
+ *    CUDA-core path in fp32 (also available for BF16 via LAGA_VARIANT_SIMT).
+ *  - batch, Sq, Skv >= 1, n_h >= 1, 0 <= q_offset, and q_offset + Sq <= Skv
+ *    when causal.
+ */
+#ifndef LAGA_MLA_H
+#define LAGA_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st* laga_stream_t;
+
+typedef enum {
+  LAGA_OK = 0,
+  LAGA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad sizes, q_offset+Sq > Skv when causal */
+  LAGA_ERR_UNSUPPORTED = 2, /* sizes or dtype this build has no kernel for */
+  LAGA_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than the query function said */
+  LAGA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or kernel launch failed */
+  LAGA_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (reported by laga_mla_check) */
+} laga_status;
+
+typedef enum { LAGA_DTYPE_F32 = 0, LAGA_DTYPE_BF16 = 1 } laga_dtype;
+
+/* How K and V reach the attention kernels.
+ *  MATERIALIZE: one tensor-core GEMM writes every head's K_nope and V to the
+ *               workspace in HBM, the attention kernels read them back.
+ *  FUSED_RECON: forward only — each attention CTA rebuilds its K_nope/V tiles
+ *               from the latent tile on the tensor cores, nothing is written.
+ *  SIMT:        the fp32 CUDA-core kernels (any dims).
+ *  AUTO:        MATERIALIZE for the supported BF16 dims, else SIMT. */
+typedef enum {
+  LAGA_VARIANT_AUTO = 0,
+  LAGA_VARIANT_MATERIALIZE = 1,
+  LAGA_VARIANT_FUSED_RECON = 2,
+  LAGA_VARIANT_SIMT = 3
+} laga_variant;
+
+typedef struct {
+  int64_t batch;     /* B */
+  int64_t sq;        /* local query rows of this SP rank */
+  int64_t skv;       /* gathered latent length S */
+  int64_t n_h;       /* heads */
+  int64_t d_c;       /* latent width */
+  int64_t d_nope;    /* per-head no-RoPE query/key width */
+  int64_t d_rope;    /* RoPE query/key width (key shared by all heads) */
+  int64_t d_v;       /* per-head value width */
+  int64_t q_offset;  /* absolute position of local query row 0 */
+  int32_t causal;    /* nonzero: key j visible to local query i iff j <= q_offset + i */
+  float softmax_scale; /* <= 0 selects 1/sqrt(d_nope + d_rope) */
+  int32_t dtype;     /* laga_dtype */
+  int32_t variant;   /* laga_variant */
+} laga_mla_desc;
+
+/* Bytes of device workspace laga_mla_fwd / laga_mla_bwd need for this
+ * problem (0 if the descriptor is invalid or unsupported). The workspace must
+ * be 256-byte aligned and must not be shared by calls in flight. */
+size_t laga_mla_fwd_workspace_size(const laga_mla_desc* desc);
+size_t laga_mla_bwd_workspace_size(const laga_mla_desc* desc);
+
+/* Forward: out [B,Sq,n_h,d_v] (dtype) and lse [B,n_h,Sq] (fp32).
+ * All pointers are device pointers. */
+laga_status laga_mla_fwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
+                         const void* W_UK, const void* W_UV, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, laga_stream_t stream);
+
+/* Backward of the loss <dout, out>. out and lse are the forward's outputs for
+ * the same inputs. Writes dq, dc_kv, dk_rope, dW_UK, dW_UV (all dtype, shapes of
+ * their primals). All pointers are device pointers. */
+laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
+                         const void* W_UK, const void* W_UV, const void* out, const float* lse,
+                         const void* dout, void* dq, void* dc_kv, void* dk_rope, void* dW_UK, void* dW_UV,
+                         void* workspace, size_t workspace_bytes, laga_stream_t stream);
+
+/* Step 1 alone (LAGA's local K/V rebuild): k_nope [B,Skv,n_h,d_nope] and
+ * v [B,Skv,n_h,d_v] from c_kv, W_UK, W_UV, for all Skv rows. Device pointers.
+ * Needs no workspace. */
+laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
+                                 const void* W_UV, void* k_nope, void* v, laga_stream_t stream);
+
+/* Synchronises the stream, then reads and clears this device's status word.
+ * Returns LAGA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * check, LAGA_ERR_CUDA if the stream reports an error, else LAGA_OK. */
+laga_status laga_mla_check(laga_stream_t stream);
+
+/* Static string naming a status code. */
+const char* laga_status_string(laga_status status);
+
+/* Detail of the last error returned on this host thread (static storage). */
+const char* laga_mla_last_error(void);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int laga_mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAGA_MLA_H */

@@ -1,0 +1,407 @@
+// Causal attention forward on the tensor cores for the LAGA MLA block:
+// d_qk = 128 (no-RoPE) + 64 (RoPE), d_v = 128, bf16 operands, fp32 softmax.
+//
+// One CTA per (128-row query tile, head, batch element); keys stream in
+// 128-row tiles. The RoPE-key concat of each head is never materialised:
+// S = Q K^T is the sum of the no-RoPE product (K = 128) and the RoPE product
+// against the shared k_rope tile (K = 64), accumulated into one TMEM tile.
+//
+// Warp roles (192 threads):
+//   warp 0      lane 0: TMA for Q and K tiles; lane 1: TMA for V tiles
+//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
+//   warps 2..5  softmax: one query row per thread (TMEM lane), online max and
+//               sum in the log2 domain, P written back over S as bf16 pairs,
+//               O rescaled in TMEM when the running max grows, final epilogue
+// TMEM columns: S/P buffer 0 [0,128), S/P buffer 1 [128,256), O [256,384).
+// MMA order S(0), S(1), PV(0), S(2), PV(1), ... lets softmax of tile j+1
+// overlap the PV product of tile j.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace laga {
+namespace {
+
+constexpr int BQ = 128;
+constexpr int BKV = 128;
+constexpr int BOX = 16384;  // one [128 rows][64 cols] bf16 box
+constexpr int Q_BYTES = 3 * BOX;
+constexpr int K_BYTES = 3 * BOX;
+constexpr int V_BYTES = 2 * BOX;
+constexpr int SMEM_BYTES = Q_BYTES + 2 * K_BYTES + 2 * V_BYTES + 1024 + 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_O = 256;
+constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, false, true);
+constexpr float LOG2E = 1.4426950408889634f;
+// The running max is only raised (and O rescaled) once it has grown by more
+// than this many powers of two; exact, since numerator and denominator share
+// the stale max.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+struct FwdParams {
+  int* status;  // device status word (timeouts)
+  int Sq, S, n_h, q_offset, causal, skv_pad, n_q_tiles;
+  float scale_log2;  // softmax scale * log2(e)
+  bf16* out;
+  float* lse;
+};
+
+__device__ __forceinline__ int n_kv_tiles(const FwdParams& p, int t) {
+  const int last = p.causal ? p.q_offset + min(p.Sq, (t + 1) * BQ) - 1 : p.S - 1;
+  return last / BKV + 1;
+}
+
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
+                    const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + Q_BYTES;
+  uint8_t* sV = sK + 2 * K_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * V_BYTES);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2]
+  uint64_t* p_full = bars + 11;  // [2]
+  uint64_t* pv_done = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // Heaviest query tiles (most key tiles) first.
+  const int t = p.n_q_tiles - 1 - static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int n_kv = n_kv_tiles(p, t);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+    }
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mR);
+      mbar_arrive_expect_tx(q_full, Q_BYTES);
+      const int qc = h * 192;
+      tma_load_3d(sQ, &mQ, q_full, qc, t * BQ, b);
+      tma_load_3d(sQ + BOX, &mQ, q_full, qc + 64, t * BQ, b);
+      tma_load_3d(sQ + 2 * BOX, &mQ, q_full, qc + 128, t * BQ, b);
+      int j = 0;
+      for (; j < n_kv; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait_or_abort(&k_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, 11)) break;
+        uint8_t* dst = sK + s * K_BYTES;
+        mbar_arrive_expect_tx(&k_full[s], K_BYTES);
+        const int row = b * p.skv_pad + j * BKV;
+        tma_load_2d(dst, &mK, &k_full[s], h * 128, row);
+        tma_load_2d(dst + BOX, &mK, &k_full[s], h * 128 + 64, row);
+        tma_load_3d(dst + 2 * BOX, &mR, &k_full[s], 0, j * BKV, b);
+      }
+      if (j < n_kv) {  // aborted: let issued copies land
+        mbar_drain(q_full, 0);
+        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&k_full[i & 1], (i >> 1) & 1);
+      }
+    } else if (lane == 1) {
+      tma_prefetch_desc(&mV);
+      int j = 0;
+      for (; j < n_kv; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait_or_abort(&v_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, 12)) break;
+        uint8_t* dst = sV + s * V_BYTES;
+        mbar_arrive_expect_tx(&v_full[s], V_BYTES);
+        const int row = b * p.skv_pad + j * BKV;
+        tma_load_2d(dst, &mV, &v_full[s], h * 128, row);
+        tma_load_2d(dst + BOX, &mV, &v_full[s], h * 128 + 64, row);
+      }
+      if (j < n_kv)
+        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&v_full[i & 1], (i >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait_or_abort(q_full, 0, abort_flag, 13);
+      bool issued = false;
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(sQ);
+      auto issue_pv = [&](int jj) -> bool {
+        const int s = jj & 1;
+        const uint32_t ph = (jj >> 1) & 1;
+        if (!mbar_wait_or_abort(&p_full[s], ph, abort_flag, 14)) return false;
+        if (!mbar_wait_or_abort(&v_full[s], ph, abort_flag, 15)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(sV + s * V_BYTES);
+        const uint32_t p_tmem = tmem + s * 128;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(v_base + kk * 2048, BOX, 1024);
+          mma_ts(tmem + COL_O, p_tmem + kk * 8, bd, IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(pv_done);
+        mma_commit(&v_empty[s]);
+        return true;
+      };
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait_or_abort(&k_full[s], (j >> 1) & 1, abort_flag, 16)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(sK + s * K_BYTES);
+        const uint32_t d_tmem = tmem + s * 128;
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint32_t c = kk >> 2, k = kk & 3;
+          const uint64_t ad = sdesc_sw128(q_base + c * BOX + k * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_base + c * BOX + k * 32, 16, 1024);
+          mma_ss(d_tmem, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        issued = true;
+        mma_commit(&s_full[s]);
+        mma_commit(&k_empty[s]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) ok = issue_pv(n_kv - 1);
+      if (!ok && issued) {
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {
+    // ---------------- softmax warpgroup: thread owns query row r of the tile
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int q_row = t * BQ + r;  // local query index
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int limit = p.causal ? p.q_offset + q_row : p.S - 1;  // last visible key
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    int pv_seen = 0;  // PV completions observed on pv_done
+    bool ok = true;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+      bool w = true;
+      if (lane == 0) w = mbar_wait_or_abort(bar, parity, abort_flag, where);
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    auto wait_pv = [&](int upto) -> bool {  // until PV(upto) has completed
+      while (pv_seen <= upto) {
+        if (!warp_wait(pv_done, pv_seen & 1, 17)) return false;
+        ++pv_seen;
+      }
+      return true;
+    };
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int s = j & 1;
+      if (j >= 2 && !wait_pv(j - 2)) {
+        ok = false;
+        break;
+      }
+      if (!warp_wait(&s_full[s], (j >> 1) & 1, 18)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t s_addr = tmem + s * 128 + lane_off;
+      float x[128];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(s_addr + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[i]) * p.scale_log2;
+        }
+      }
+      const int kv0 = j * BKV;
+      if (kv0 + BKV - 1 > limit) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (kv0 + i > limit) x[i] = -INFINITY;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
+      float m_use = m_run;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_run == -INFINITY) {
+        m_use = mt;
+      } else if (mt > m_run + RESCALE_THRESHOLD) {
+        m_use = mt;
+        alpha = ex2_approx(m_run - mt);
+        rescale = true;
+      }
+      // rows with nothing visible yet keep p = 0
+      const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2_approx(x[2 * i] - m_sub);
+        const float p1 = ex2_approx(x[2 * i + 1] - m_sub);
+        sum += p0 + p1;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_use;
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = pk[c * 32 + i];
+          tmem_st32(s_addr + c * 32, w);
+        }
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O may only be touched once PV(j-1) has landed.
+        if (!wait_pv(j - 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t o_addr = tmem + COL_O + lane_off;
+        uint32_t u[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(o_addr + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(o_addr + c * 32, u);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[s]);
+    }
+    if (ok && wait_pv(n_kv - 1)) {
+      tc_fence_after();
+      const uint32_t o_addr = tmem + COL_O + lane_off;
+      const bool valid = q_row < p.Sq;
+      const float inv = 1.f / l_run;
+      bf16* orow = p.out + ((static_cast<long long>(b) * p.Sq + q_row) * p.n_h + h) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(o_addr + c * 32, u);
+        tmem_wait_ld();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
+            dst[v] = w;
+          }
+        }
+      }
+      if (valid)
+        p.lse[(static_cast<long long>(b) * p.n_h + h) * p.Sq + q_row] =
+            (m_run + __log2f(l_run)) * 0.6931471805599453f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) publish_abort(abort_flag, p.status);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+// The [rows][64] boxes of the operands: 3D q map over [B][Sq][n_h*192], 2D maps
+// over the [B*skv_pad][n_h*128] K/V workspace, 3D k_rope map over [B][S][64].
+LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const bf16* v_ws, const bf16* k_rope,
+                         bf16* out, float* lse, cudaStream_t st) {
+  LaunchResult r;
+  CUtensorMap mQ, mK, mR, mV;
+  {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 192;
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
+    const uint32_t box[3] = {64, 128, 1};
+    r.cu = make_tmap(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t kv_inner = static_cast<uint64_t>(d.n_h) * 128;
+  const uint64_t kv_rows = static_cast<uint64_t>(d.B) * d.skv_pad;
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t dims[2] = {kv_inner, kv_rows};
+    const uint64_t strides[1] = {kv_inner * 2};
+    const uint32_t box[2] = {64, 128};
+    r.cu = make_tmap(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_ws, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r.cu == CUDA_SUCCESS)
+      r.cu = make_tmap(&mV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v_ws, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(d.S), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(d.S) * 128};
+    const uint32_t box[3] = {64, 128, 1};
+    r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor maps attention forward";
+    return r;
+  }
+  FwdParams p{};
+  p.Sq = d.Sq;
+  p.S = d.S;
+  p.n_h = d.n_h;
+  p.q_offset = d.q_offset;
+  p.causal = d.causal ? 1 : 0;
+  p.skv_pad = d.skv_pad;
+  p.n_q_tiles = (d.Sq + BQ - 1) / BQ;
+  p.scale_log2 = d.scale * LOG2E;
+  p.out = out;
+  p.lse = lse;
+  p.status = device_status_ptr();
+  r.err = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (r.err != cudaSuccess) {
+    r.what = "cudaFuncSetAttribute(attn_fwd)";
+    return r;
+  }
+  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), 192, SMEM_BYTES, st>>>(mQ, mK, mR, mV, p);
+  r.err = cudaGetLastError();
+  if (r.err != cudaSuccess) r.what = "attn_fwd_kernel launch";
+  return r;
+}
+
+}  // namespace laga

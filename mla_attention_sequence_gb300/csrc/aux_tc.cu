@@ -1,0 +1,163 @@
+// Workspace layout and the small memory-bound kernels around the tensor-core
+// attention backward:
+//   pre   D_i = dout_i . out_i and lse in the log2 domain, padded per (b, h) row;
+//         dq accumulator cleared
+//   post  dq = scale * accumulated dS K (fp32 -> bf16); dk_rope = sum over
+//         heads of the per-head RoPE-key gradients (the RoPE key is one tensor
+//         shared by every head, so its gradient collects all of them)
+#include "internal.h"
+
+namespace laga {
+
+bool tc_supported(const Dims& d) { return d.d_c == 512 && d.d_nope == 128 && d.d_v == 128 && d.d_rope == 64; }
+
+namespace {
+size_t kv_ws_bytes(const Dims& d) { return align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 128 * 2, 256); }
+}  // namespace
+
+size_t tc_fwd_workspace(const Dims& d) { return 2 * kv_ws_bytes(d); }
+
+size_t tc_bwd_workspace(const Dims& d) {
+  const size_t kv = kv_ws_bytes(d);
+  const size_t dkr = align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 64 * 4, 256);
+  const size_t dq = align_up(static_cast<size_t>(d.B) * d.Sq * d.n_h * 192 * 4, 256);
+  const size_t rows = align_up(static_cast<size_t>(d.B) * d.n_h * d.sq_pad * 4, 256);
+  return 4 * kv + dkr + dq + 2 * rows;
+}
+
+BwdWorkspace tc_bwd_carve(const Dims& d, void* ws) {
+  char* p = static_cast<char*>(ws);
+  const size_t kv = kv_ws_bytes(d);
+  BwdWorkspace w{};
+  w.k_ws = reinterpret_cast<bf16*>(p);
+  p += kv;
+  w.v_ws = reinterpret_cast<bf16*>(p);
+  p += kv;
+  w.dk_ws = reinterpret_cast<bf16*>(p);
+  p += kv;
+  w.dv_ws = reinterpret_cast<bf16*>(p);
+  p += kv;
+  w.dkr_ws = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 64 * 4, 256);
+  w.dq_acc = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(d.B) * d.Sq * d.n_h * 192 * 4, 256);
+  w.lse2 = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(d.B) * d.n_h * d.sq_pad * 4, 256);
+  w.delta = reinterpret_cast<float*>(p);
+  return w;
+}
+
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+// One warp per (b, h, i) row of the padded [B][n_h][sq_pad] arrays.
+__global__ void bwd_pre_kernel(Dims d, const bf16* __restrict__ out, const bf16* __restrict__ dout,
+                               const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta) {
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long rows = static_cast<long long>(d.B) * d.n_h * d.sq_pad;
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int i = static_cast<int>(row % d.sq_pad);
+  const long long bh = row / d.sq_pad;
+  const int h = static_cast<int>(bh % d.n_h);
+  const int b = static_cast<int>(bh / d.n_h);
+  if (i >= d.Sq) {
+    if (lane == 0) {
+      lse2[row] = INFINITY;
+      delta[row] = 0.f;
+    }
+    return;
+  }
+  const long long off = ((static_cast<long long>(b) * d.Sq + i) * d.n_h + h) * 128 + lane * 4;
+  const uint2 a = *reinterpret_cast<const uint2*>(out + off);
+  const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
+  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float2 af = __bfloat1622float2(a2[k]);
+    const float2 gf = __bfloat1622float2(g2[k]);
+    acc = fmaf(af.x, gf.x, acc);
+    acc = fmaf(af.y, gf.y, acc);
+  }
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    delta[row] = acc;
+    lse2[row] = lse[(static_cast<long long>(b) * d.n_h + h) * d.Sq + i] * LOG2E;
+  }
+}
+
+__global__ void dq_convert_kernel(long long n4, float scale, const float4* __restrict__ acc,
+                                  uint2* __restrict__ dq) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = acc[i];
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t*>(&lo);
+  o.y = *reinterpret_cast<uint32_t*>(&hi);
+  dq[i] = o;
+}
+
+// dk_rope[b, j, :] = sum_h dkr[b, j, h, :]; 16 threads x 4 columns per row.
+__global__ void rope_sum_kernel(Dims d, const float* __restrict__ dkr, bf16* __restrict__ dk_rope) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(d.B) * d.S * 16;
+  if (t >= total) return;
+  const int c4 = static_cast<int>(t % 16);
+  const long long bj = t / 16;
+  const int j = static_cast<int>(bj % d.S);
+  const int b = static_cast<int>(bj / d.S);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (j < d.skv_pad) {
+    const float4* src =
+        reinterpret_cast<const float4*>(dkr + ((static_cast<long long>(b) * d.skv_pad + j) * d.n_h) * 64) + c4;
+    for (int h = 0; h < d.n_h; ++h) {
+      const float4 v = src[h * 16];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t*>(&lo);
+  o.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(dk_rope + (static_cast<long long>(b) * d.S + j) * 64)[c4] = o;
+}
+
+}  // namespace
+
+LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const float* lse, const BwdWorkspace& w,
+                        cudaStream_t st) {
+  LaunchResult r;
+  r.err = cudaMemsetAsync(w.dq_acc, 0, static_cast<size_t>(d.B) * d.Sq * d.n_h * 192 * 4, st);
+  if (r.err != cudaSuccess) {
+    r.what = "clear dq accumulator";
+    return r;
+  }
+  const long long rows = static_cast<long long>(d.B) * d.n_h * d.sq_pad;
+  bwd_pre_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(d, out, dout, lse, w.lse2, w.delta);
+  r.err = cudaGetLastError();
+  if (r.err != cudaSuccess) r.what = "bwd_pre_kernel";
+  return r;
+}
+
+LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dq, bf16* dk_rope, cudaStream_t st) {
+  LaunchResult r;
+  const long long n4 = static_cast<long long>(d.B) * d.Sq * d.n_h * 192 / 4;
+  dq_convert_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
+      n4, d.scale, reinterpret_cast<const float4*>(w.dq_acc), reinterpret_cast<uint2*>(dq));
+  const long long t = static_cast<long long>(d.B) * d.S * 16;
+  rope_sum_kernel<<<static_cast<unsigned>((t + 255) / 256), 256, 0, st>>>(d, w.dkr_ws, dk_rope);
+  r.err = cudaGetLastError();
+  if (r.err != cudaSuccess) r.what = "bwd post kernels";
+  return r;
+}
+
+}  // namespace laga

@@ -1,0 +1,412 @@
+// Tensor-core (tcgen05 + TMEM + TMA) GEMMs of the K/V reconstruction and its
+// backward, for bf16 operands with fp32 accumulation:
+//
+//   RECON_FWD  K_nope = c_kv W_UK, V = c_kv W_UV           per batch element
+//              (LAGA: per-head K/V rebuilt locally from the gathered latent)
+//   DCKV       dc_kv = dK_nope W_UK^T + dV W_UV^T          per batch element
+//   DW         dW_UK = sum_b c_kv[b]^T dK_nope[b], dW_UV likewise
+//
+// One persistent kernel template serves all three. Warp roles (192 threads):
+//   warp 0      TMA producer into a STAGES-deep shared-memory ring
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2..5  epilogue: TMEM -> registers -> bf16 -> global
+// Two TMEM accumulators let the epilogue of one tile overlap the next tile's
+// main loop. Operand tiles use the 128-byte swizzle; a K-major tile is
+// [rows][64 K] (128-byte rows), an MN-major tile is a set of [64 K][64 MN] boxes.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <algorithm>
+
+namespace laga {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+enum Mode { RECON_FWD = 0, DCKV = 1, DW = 2 };
+
+struct GemmParams {
+  int* status;  // device status word (timeouts)
+  int m_tiles, n_tiles, batches;  // tiles = m_tiles * n_tiles * batches, n fastest
+  int n_tiles_first;              // RECON_FWD / DW: n tiles served by operand pair 0
+  int k_blocks;                   // BK-blocks per tile
+  int kb_first;                   // DCKV: k blocks served by pair 0 (dK_nope . W_UK^T)
+  int kb_per_batch;               // DW: k blocks per batch element
+  int S, skv_pad;
+  bf16* out0;
+  bf16* out1;
+  long long ldo;               // elements per output row
+  long long out_batch_stride;  // elements between batch elements of the output
+  int rows_valid;              // output rows (per batch element) that exist
+};
+
+template <int MODE, int BN, int STAGES>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr bool A_MN = (MODE == DW);
+  static constexpr bool B_MN = (MODE != DCKV);
+  static constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+  static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
+  static_assert(BN % 64 == 0 && BN <= 256, "BN");
+};
+
+template <int MODE, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
+                   const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+                   const GemmParams p) {
+  using C = Cfg<MODE, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = bars + 2 * STAGES + 2;
+  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int tiles_per_batch = p.m_tiles * p.n_tiles;
+  const int num_tiles = tiles_per_batch * p.batches;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA0);
+      tma_prefetch_desc(&mapA1);
+      tma_prefetch_desc(&mapB0);
+      tma_prefetch_desc(&mapB1);
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int b = tile / tiles_per_batch;
+        const int rem = tile - b * tiles_per_batch;
+        const int m = rem / p.n_tiles;
+        const int n = rem - m * p.n_tiles;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_or_abort(&empty[s], ph ^ 1, abort_flag, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          uint8_t* a = sA + s * C::A_BYTES;
+          uint8_t* bsm = sB + s * C::B_BYTES;
+          if constexpr (MODE == RECON_FWD) {
+            const bool second = n >= p.n_tiles_first;
+            const int n0 = (second ? n - p.n_tiles_first : n) * BN;
+            tma_load_3d(a, &mapA0, &full[s], kb * BK, m * BM, b);
+            const CUtensorMap* mb = second ? &mapB1 : &mapB0;
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_2d(bsm + i * 8192, mb, &full[s], n0 + 64 * i, kb * BK);
+          } else if constexpr (MODE == DCKV) {
+            const bool second = kb >= p.kb_first;
+            const int kk = second ? kb - p.kb_first : kb;
+            tma_load_2d(a, second ? &mapA1 : &mapA0, &full[s], kk * BK, b * p.skv_pad + m * BM);
+            tma_load_2d(bsm, second ? &mapB1 : &mapB0, &full[s], kk * BK, n * BN);
+          } else {
+            const bool second = n >= p.n_tiles_first;
+            const int n0 = (second ? n - p.n_tiles_first : n) * BN;
+            const int bb = kb / p.kb_per_batch;
+            const int kk = kb - bb * p.kb_per_batch;
+            tma_load_2d(a, &mapA0, &full[s], m * BM, bb * p.S + kk * BK);
+            tma_load_2d(a + 8192, &mapA0, &full[s], m * BM + 64, bb * p.S + kk * BK);
+            const CUtensorMap* mb = second ? &mapB1 : &mapB0;
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(bsm + i * 8192, mb, &full[s], n0 + 64 * i, bb * p.skv_pad + kk * BK);
+          }
+        }
+      }
+      if (!ok) {
+        // Let copies already in flight land before shared memory goes away.
+        const int first = it > STAGES ? it - STAGES : 0;
+        for (int j = first; j < it; ++j) mbar_drain(&full[j % STAGES], (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0;
+      int local = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait_or_abort(&acc_empty[buf], (use & 1) ^ 1, abort_flag, 2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait_or_abort(&full[s], ph, abort_flag, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = C::A_MN ? sdesc_sw128(a_base + k * 2048, 8192, 1024)
+                                        : sdesc_sw128(a_base + k * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? sdesc_sw128(b_base + k * 2048, 8192, 1024)
+                                        : sdesc_sw128(b_base + k * 32, 16, 1024);
+            mma_ss(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&acc_full[buf]);
+      }
+      if (!ok && issued) {
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {
+    // Epilogue warps 2..5: warp (w % 4) may read TMEM lanes 32*(w%4) .. +31.
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_or_abort(&acc_full[buf], use & 1, abort_flag, 4);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int b = tile / tiles_per_batch;
+      const int rem = tile - b * tiles_per_batch;
+      const int m = rem / p.n_tiles;
+      const int n = rem - m * p.n_tiles;
+      bf16* out;
+      int n0;
+      if constexpr (MODE == DCKV) {
+        out = p.out0;
+        n0 = n * BN;
+      } else {
+        const bool second = n >= p.n_tiles_first;
+        out = second ? p.out1 : p.out0;
+        n0 = (second ? n - p.n_tiles_first : n) * BN;
+      }
+      const int row = m * BM + row_in_tile;
+      const bool valid = row < p.rows_valid;
+      bf16* orow = out + static_cast<long long>(b) * p.out_batch_stride + static_cast<long long>(row) * p.ldo + n0;
+      const uint32_t t_row = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(t_row + c0, r);
+        tmem_wait_ld();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+            dst[v] = w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) publish_abort(abort_flag, p.status);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <int MODE, int BN, int STAGES>
+LaunchResult launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                         const CUtensorMap& b1, const GemmParams& p, cudaStream_t st) {
+  using C = Cfg<MODE, BN, STAGES>;
+  LaunchResult r;
+  auto kern = gemm_tc_kernel<MODE, BN, STAGES>;
+  r.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (r.err != cudaSuccess) {
+    r.what = "cudaFuncSetAttribute(gemm)";
+    return r;
+  }
+  const int tiles = p.m_tiles * p.n_tiles * p.batches;
+  if (tiles == 0) return r;
+  const int grid = std::min(tiles, sm_count());
+  GemmParams pp = p;
+  pp.status = device_status_ptr();
+  kern<<<grid, 192, C::SMEM, st>>>(a0, a1, b0, b1, pp);
+  r.err = cudaGetLastError();
+  if (r.err != cudaSuccess) r.what = "gemm_tc_kernel launch";
+  return r;
+}
+
+CUresult tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_outer) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {row_bytes};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, const bf16* W_UV, bf16* k_ws,
+                          bf16* v_ws, int rows_pad, cudaStream_t st) {
+  constexpr int BN = 256;
+  LaunchResult r;
+  CUtensorMap a0, b0, b1;
+  const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(d.d_c), static_cast<uint64_t>(d.S),
+                              static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(d.d_c) * 2, static_cast<uint64_t>(d.S) * d.d_c * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    r.cu = make_tmap(&a0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c_kv, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r.cu != CUDA_SUCCESS) {
+      r.what = "tensor map c_kv";
+      return r;
+    }
+  }
+  r.cu = tmap_bf16_2d(&b0, W_UK, N, d.d_c, N * 2, 64, 64);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b1, W_UV, N, d.d_c, N * 2, 64, 64);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor map W";
+    return r;
+  }
+  GemmParams p{};
+  p.m_tiles = rows_pad / BM;
+  p.n_tiles_first = static_cast<int>(N / BN);
+  p.n_tiles = 2 * p.n_tiles_first;
+  p.batches = d.B;
+  p.k_blocks = d.d_c / BK;
+  p.S = d.S;
+  p.skv_pad = rows_pad;
+  p.out0 = k_ws;
+  p.out1 = v_ws;
+  p.ldo = static_cast<long long>(N);
+  p.out_batch_stride = static_cast<long long>(rows_pad) * N;
+  p.rows_valid = rows_pad;
+  return launch_gemm<RECON_FWD, BN, 4>(a0, a0, b0, b1, p, st);
+}
+
+LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws, const bf16* W_UK,
+                             const bf16* W_UV, bf16* dc_kv, cudaStream_t st) {
+  constexpr int BN = 128;
+  LaunchResult r;
+  CUtensorMap a0, a1, b0, b1;
+  const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;  // reduction length of each pair
+  const uint64_t rows = static_cast<uint64_t>(d.B) * d.skv_pad;
+  r.cu = tmap_bf16_2d(&a0, dk_ws, N, rows, N * 2, 64, 128);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&a1, dv_ws, N, rows, N * 2, 64, 128);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b0, W_UK, N, d.d_c, N * 2, 64, BN);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b1, W_UV, N, d.d_c, N * 2, 64, BN);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor maps dc_kv";
+    return r;
+  }
+  GemmParams p{};
+  p.m_tiles = d.skv_pad / BM;
+  p.n_tiles = d.d_c / BN;
+  p.n_tiles_first = p.n_tiles;
+  p.batches = d.B;
+  p.kb_first = static_cast<int>(N / BK);
+  p.k_blocks = 2 * p.kb_first;
+  p.S = d.S;
+  p.skv_pad = d.skv_pad;
+  p.out0 = dc_kv;
+  p.out1 = dc_kv;
+  p.ldo = d.d_c;
+  p.out_batch_stride = static_cast<long long>(d.S) * d.d_c;
+  p.rows_valid = d.S;
+  return launch_gemm<DCKV, BN, 6>(a0, a1, b0, b1, p, st);
+}
+
+LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws, const bf16* dv_ws, bf16* dW_UK,
+                             bf16* dW_UV, cudaStream_t st) {
+  constexpr int BN = 256;
+  LaunchResult r;
+  CUtensorMap a0, b0, b1;
+  const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;
+  r.cu = tmap_bf16_2d(&a0, c_kv, d.d_c, static_cast<uint64_t>(d.B) * d.S, static_cast<uint64_t>(d.d_c) * 2, 64,
+                      64);
+  const uint64_t rows = static_cast<uint64_t>(d.B) * d.skv_pad;
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b0, dk_ws, N, rows, N * 2, 64, 64);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b1, dv_ws, N, rows, N * 2, 64, 64);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor maps dW";
+    return r;
+  }
+  GemmParams p{};
+  p.m_tiles = d.d_c / BM;
+  p.n_tiles_first = static_cast<int>(N / BN);
+  p.n_tiles = 2 * p.n_tiles_first;
+  p.batches = 1;
+  p.kb_per_batch = d.skv_pad / BK;
+  p.k_blocks = p.kb_per_batch * d.B;
+  p.S = d.S;
+  p.skv_pad = d.skv_pad;
+  p.out0 = dW_UK;
+  p.out1 = dW_UV;
+  p.ldo = static_cast<long long>(N);
+  p.out_batch_stride = 0;
+  p.rows_valid = d.d_c;
+  return launch_gemm<DW, BN, 4>(a0, a0, b0, b1, p, st);
+}
+
+}  // namespace laga

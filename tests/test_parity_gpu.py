@@ -1,0 +1,235 @@
+"""GPU path vs the fp64 oracle, through the C ABI, on the same seeded inputs.
+
+Tolerances (per output tensor): max|gpu - oracle| <= 1e-4 * max|oracle| for fp32
+problems and <= 2e-2 * max|oracle| for bf16 problems.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_attention_sequence_gb300 import laga
+from mla_attention_sequence_gb300.configs import DSV3_LAST_RANK, MID_BF16, TINY_F32, Problem
+from mla_attention_sequence_gb300.synth import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+KEYS = ("out", "lse", "dq", "dc_kv", "dk_rope", "dW_UK", "dW_UV")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mla_attention_sequence_gb300 import build
+    build.build()
+    laga.lib()
+
+
+def dev():
+    return torch.device("cuda", 0)
+
+
+def to_dev(x, p):
+    dt = torch.float32 if p.dtype == "f32" else torch.bfloat16
+    return {k: torch.from_numpy(v).to(dev()).to(dt).contiguous() for k, v in x.items()}
+
+
+def np64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(p, x, variant="auto", backward=True):
+    t = to_dev(x, p)
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal, None, variant)
+    res = {"out": out, "lse": lse}
+    if backward:
+        res.update(laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset,
+                            p.causal, None, "auto" if variant == "fused_recon" else variant))
+    laga.check(dev())
+    return res
+
+
+def run_oracle(p, x, backward=True):
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    out, lse = oracle.mla_forward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], p.q_offset,
+                                  p.causal)
+    ref = {"out": out, "lse": lse}
+    if backward:
+        ref.update(oracle.mla_backward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
+                                       p.q_offset, p.causal))
+    return ref
+
+
+def assert_close(got, ref, tol, keys=None, tag=""):
+    bad = []
+    for k in keys or ref.keys():
+        a = np64(got[k]) if torch.is_tensor(got[k]) else got[k]
+        r = ref[k]
+        assert a.shape == r.shape, (k, a.shape, r.shape)
+        assert np.isfinite(a).all(), f"{tag} {k}: non-finite values"
+        err = np.abs(a - r).max()
+        bound = tol * max(np.abs(r).max(), 1e-30)
+        if not err <= bound:
+            bad.append(f"{k}: max|err|={err:.3e} > {bound:.3e}")
+    assert not bad, f"{tag} " + "; ".join(bad)
+
+
+def small(**kw):
+    base = dict(B=1, Sq=256, S=256, n_h=2, d_c=512, d_nope=128, d_rope=64, d_v=128, q_offset=0, causal=True,
+                dtype="bf16")
+    base.update(kw)
+    return Problem(**base)
+
+
+# ------------------------------------------------------------------ CUDA-core path
+def test_tiny_f32_forward_backward():
+    p = TINY_F32
+    x = make_inputs(p, seed=0)
+    assert_close(run_gpu(p, x), run_oracle(p, x), TOL["f32"], tag="tiny f32")
+
+
+@pytest.mark.parametrize("kw", [dict(q_offset=5, Sq=11, S=23, causal=True), dict(q_offset=0, Sq=9, S=14, causal=False)])
+def test_simt_f32_ragged(kw):
+    p = Problem(B=2, n_h=3, d_c=24, d_nope=8, d_rope=4, d_v=12, dtype="f32", **kw)
+    x = make_inputs(p, seed=1)
+    assert_close(run_gpu(p, x), run_oracle(p, x), TOL["f32"], tag="simt f32 ragged")
+
+
+def test_simt_bf16_on_request():
+    p = small(Sq=70, S=150, q_offset=80, n_h=2)
+    x = make_inputs(p, seed=2)
+    assert_close(run_gpu(p, x, "simt"), run_oracle(p, x), TOL["bf16"], tag="simt bf16")
+
+
+# ------------------------------------------------------------------ tensor-core path
+def test_reconstruct_tensor_cores():
+    p = small(B=2, S=300, Sq=1, n_h=4)
+    x = make_inputs(p, seed=3, with_dout=False)
+    t = to_dev(x, p)
+    kn, v = laga.reconstruct(t["c_kv"], t["W_UK"], t["W_UV"], p.n_h)
+    laga.check(dev())
+    rk, rv = oracle.reconstruct(x["c_kv"].astype(np.float64), x["W_UK"].astype(np.float64),
+                                x["W_UV"].astype(np.float64), p.n_h)
+    # K/V come out of one bf16 rounding of an fp32 accumulation: 2^-8 relative
+    for a, r in ((kn, rk), (v, rv)):
+        err = np.abs(np64(a) - r)
+        assert (err <= 2.0 ** -8 * np.abs(r) + 1e-3 * np.abs(r).max()).all()
+
+
+TC_CASES = {
+    "aligned": small(),
+    "ragged_offset": small(B=2, n_h=3, Sq=200, S=520, q_offset=300),
+    "noncausal_ragged": small(n_h=2, Sq=77, S=333, causal=False),
+    "single_query_first": small(Sq=1, S=1, q_offset=0),
+    "single_query_last": small(Sq=1, S=701, q_offset=700),
+    "multi_tile": small(B=1, n_h=2, Sq=384, S=1000, q_offset=600),
+}
+
+
+@pytest.mark.parametrize("name", list(TC_CASES))
+def test_tensor_core_forward(name):
+    p = TC_CASES[name]
+    x = make_inputs(p, seed=10)
+    assert_close(run_gpu(p, x, "materialize", backward=False), run_oracle(p, x, backward=False), TOL["bf16"],
+                 tag=name)
+
+
+@pytest.mark.parametrize("name", list(TC_CASES))
+def test_tensor_core_backward(name):
+    p = TC_CASES[name]
+    x = make_inputs(p, seed=11)
+    assert_close(run_gpu(p, x, "materialize"), run_oracle(p, x), TOL["bf16"], tag=name)
+
+
+def test_mid_config_full_parity():
+    p = MID_BF16
+    x = make_inputs(p, seed=1000)
+    assert_close(run_gpu(p, x), run_oracle(p, x), TOL["bf16"], tag="mid")
+
+
+def test_lse_and_out_of_padded_rows_are_untouched():
+    """Rows beyond Sq are never written; the tensors keep what the caller put there."""
+    p = small(Sq=130, S=400, q_offset=200)
+    x = make_inputs(p, seed=12)
+    t = to_dev(x, p)
+    out = torch.full((p.B, p.Sq + 1, p.n_h, p.d_v), 7.0, dtype=torch.bfloat16, device=dev())
+    lse = torch.full((p.B, p.n_h, p.Sq), 7.0, device=dev())
+    o, l = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True, out=out[:, :p.Sq],
+                    lse=lse)
+    torch.cuda.synchronize()
+    assert (out[:, p.Sq:].float() == 7.0).all()
+
+
+# ------------------------------------------------------------------ full size, sampled
+def test_dsv3_last_rank_sampled_heads_and_identities():
+    """The DeepSeek-V3 SP=8 last-rank shard at full size (the benchmark's launch
+    configuration): selected heads against the per-head oracle, and the
+    gradient identities that tie dc_kv and dk_rope to the other outputs."""
+    p = DSV3_LAST_RANK
+    x = make_inputs(p, seed=2007)
+    t = to_dev(x, p)
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True)
+    g = laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True)
+    laga.check(dev())
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    for h in (0, 77, 127):
+        ref = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
+                                       0, h, p.q_offset, True)
+        got = {"out": out[0, :, h], "lse": lse[0, h], "dq": g["dq"][0, :, h],
+               "dW_UK": g["dW_UK"][:, h * 128:(h + 1) * 128], "dW_UV": g["dW_UV"][:, h * 128:(h + 1) * 128]}
+        want = {"out": ref["out_h"], "lse": ref["lse_h"], "dq": ref["dq_h"], "dW_UK": ref["dW_UK_h"],
+                "dW_UV": ref["dW_UV_h"]}
+        assert_close(got, want, TOL["bf16"], tag=f"dsv3 head {h}")
+
+    def inner(a, b):
+        return float((np64(a) * (b if isinstance(b, np.ndarray) else np64(b))).sum())
+
+    # <dW_UV, W_UV> = <dout, out>;  <dW_UK, W_UK> + <dk_rope, k_rope> = <dq, q>;
+    # <dc_kv, c_kv> = <dW_UK, W_UK> + <dW_UV, W_UV>
+    a_uv = inner(g["dW_UV"], x64["W_UV"])
+    a_uk = inner(g["dW_UK"], x64["W_UK"])
+    a_r = inner(g["dk_rope"], x64["k_rope"])
+    a_q = inner(g["dq"], x64["q"])
+    a_o = inner(t["dout"], out)
+    a_c = inner(g["dc_kv"], x64["c_kv"])
+    scale_ = max(abs(a_q), abs(a_o), 1.0)
+    assert abs(a_uv - a_o) <= 2e-2 * scale_
+    assert abs(a_uk + a_r - a_q) <= 2e-2 * scale_
+    assert abs(a_c - (a_uk + a_uv)) <= 2e-2 * scale_
+
+
+# ------------------------------------------------------------------ SP shards, determinism
+def test_sequence_parallel_shards_on_gpu():
+    S, sp = 1024, 4
+    p1 = small(B=1, n_h=2, Sq=S, S=S, q_offset=0)
+    x = make_inputs(p1, seed=13)
+    full = run_gpu(p1, x)
+    sh = S // sp
+    sums = {k: 0.0 for k in ("dc_kv", "dk_rope", "dW_UK", "dW_UV")}
+    for r in range(sp):
+        pr = p1.with_(Sq=sh, q_offset=r * sh)
+        xr = dict(x)
+        xr["q"] = np.ascontiguousarray(x["q"][:, r * sh:(r + 1) * sh])
+        xr["dout"] = np.ascontiguousarray(x["dout"][:, r * sh:(r + 1) * sh])
+        g = run_gpu(pr, xr)
+        # same tiles, same order: forward rows are bitwise those of SP=1
+        assert torch.equal(g["out"], full["out"][:, r * sh:(r + 1) * sh])
+        assert torch.equal(g["lse"], full["lse"][:, :, r * sh:(r + 1) * sh])
+        ref_dq = np64(full["dq"][:, r * sh:(r + 1) * sh])
+        assert np.abs(np64(g["dq"]) - ref_dq).max() <= 1e-2 * np.abs(ref_dq).max()
+        for k in sums:
+            sums[k] = sums[k] + np64(g[k])
+    for k in sums:
+        ref = np64(full[k])
+        assert np.abs(sums[k] - ref).max() <= 2e-2 * np.abs(ref).max(), k
+
+
+def test_determinism():
+    p = small(B=1, n_h=4, Sq=512, S=1024, q_offset=512)
+    x = make_inputs(p, seed=14)
+    a = run_gpu(p, x)
+    b = run_gpu(p, x)
+    for k in ("out", "lse", "dc_kv", "dk_rope", "dW_UK", "dW_UV"):
+        assert torch.equal(a[k], b[k]), k
+    # dq adds per-key-tile partial sums with fp32 atomics: order may vary
+    assert np.abs(np64(a["dq"]) - np64(b["dq"])).max() <= 1e-2 * np.abs(np64(a["dq"])).max()
