@@ -307,7 +307,8 @@ CUresult tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
 
 LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, const bf16* W_UV, bf16* k_ws,
                           bf16* v_ws, int rows_pad, cudaStream_t st) {
-  constexpr int BN = 256;
+  // n_h * 128 columns per weight: 256-wide tiles when they divide it, else 128.
+  const int BN = (d.n_h % 2 == 0) ? 256 : 128;
   LaunchResult r;
   CUtensorMap a0, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;
@@ -342,7 +343,8 @@ LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, con
   p.ldo = static_cast<long long>(N);
   p.out_batch_stride = static_cast<long long>(rows_pad) * N;
   p.rows_valid = rows_pad;
-  return launch_gemm<RECON_FWD, BN, 4>(a0, a0, b0, b1, p, st);
+  if (BN == 256) return launch_gemm<RECON_FWD, 256, 4>(a0, a0, b0, b1, p, st);
+  return launch_gemm<RECON_FWD, 128, 6>(a0, a0, b0, b1, p, st);
 }
 
 LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws, const bf16* W_UK,
@@ -379,7 +381,7 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
 
 LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws, const bf16* dv_ws, bf16* dW_UK,
                              bf16* dW_UV, cudaStream_t st) {
-  constexpr int BN = 256;
+  const int BN = (d.n_h % 2 == 0) ? 256 : 128;
   LaunchResult r;
   CUtensorMap a0, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;
@@ -406,7 +408,8 @@ LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws,
   p.ldo = static_cast<long long>(N);
   p.out_batch_stride = 0;
   p.rows_valid = d.d_c;
-  return launch_gemm<DW, BN, 4>(a0, a0, b0, b1, p, st);
+  if (BN == 256) return launch_gemm<DW, 256, 4>(a0, a0, b0, b1, p, st);
+  return launch_gemm<DW, 128, 6>(a0, a0, b0, b1, p, st);
 }
 
 }  // namespace laga

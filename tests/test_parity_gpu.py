@@ -102,8 +102,9 @@ def test_simt_bf16_on_request():
 
 
 # ------------------------------------------------------------------ tensor-core path
-def test_reconstruct_tensor_cores():
-    p = small(B=2, S=300, Sq=1, n_h=4)
+@pytest.mark.parametrize("n_h", [4, 3])
+def test_reconstruct_tensor_cores(n_h):
+    p = small(B=2, S=300, Sq=1, n_h=n_h)
     x = make_inputs(p, seed=3, with_dout=False)
     t = to_dev(x, p)
     kn, v = laga.reconstruct(t["c_kv"], t["W_UK"], t["W_UV"], p.n_h)
