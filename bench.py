@@ -1,0 +1,378 @@
+"""Benchmark of the LAGA MLA attention block, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Workload (default): the DeepSeek-V3-dimension MLA layer (n_h=128, d_c=512,
+d_nope=128, d_rope=64, d_v=128), sequence 16384 split over SP=8 ranks, the
+last rank's shard (2048 queries at q_offset=14336 against the full latent),
+causal, batch 1, bf16 storage with fp32 accumulation. One step = one forward
+and one backward of that shard (reconstruction, attention, attention
+backward, reconstruction backward). Inputs are seeded synthetic N(0,1) data
+(weights N(0, 1/d_c)), generated on the host.
+
+Printed: one JSON line. `value` is algorithmic TFLOP/s (fwd flops
+2*P*n_h*(d_qk+d_v) + 2*B*Skv_eff*d_c*n_h*(d_nope+d_v), bwd = 2 x fwd) summed
+over ranks; ranks run independent replicas of the shard (no collective).
+L2 is flushed (a 512 MB buffer is written) before every timed step, outside
+the step's own CUDA events.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (a subset of heads per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from mla_attention_sequence_gb300.configs import NAMED, DSV3_LAST_RANK, Problem  # noqa: E402
+from mla_attention_sequence_gb300.synth import make_inputs  # noqa: E402
+
+METRIC = "MLA attn-block fwd+bwd TFLOP/s & tokens/s, % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+SEED = 2007
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def workload_config(p: Problem, extra=None):
+    c = {"workload": p.name, "B": p.B, "Sq": p.Sq, "S": p.S, "n_h": p.n_h, "d_c": p.d_c, "d_nope": p.d_nope,
+         "d_rope": p.d_rope, "d_v": p.d_v, "q_offset": p.q_offset, "causal": p.causal, "sp": 8,
+         "flops_per_step": p.flops_step(), "tokens_per_step": p.B * p.Sq,
+         "l2": "flushed before each timed step (512 MB write)", "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity for one process)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(p: Problem, x: dict, heads: list[int]):
+    """Run the fp64 oracle's forward+backward for the given heads of batch 0.
+    Returns the algorithmic flops of that sample."""
+    import oracle
+    x64 = x if all(v.dtype == np.float64 for v in x.values()) else {k: v.astype(np.float64) for k, v in x.items()}
+    for h in heads:
+        oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"], 0, h,
+                                 p.q_offset, p.causal)
+    return p.with_(n_h=len(heads), B=1).flops_step()
+
+
+def time_oracle(p: Problem, x: dict, budget_s: float = 15.0, max_heads: int = 64):
+    """Time the oracle over as many heads as fit the time budget (at least one)."""
+    x = {k: v.astype(np.float64) for k, v in x.items()}
+    t0 = time.perf_counter()
+    flops = 0
+    heads = 0
+    while heads < min(max_heads, p.n_h) and (time.perf_counter() - t0) < budget_s:
+        flops += oracle_sample(p, x, [heads])
+        heads += 1
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, heads, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, p: Problem):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    x = make_inputs(p, SEED)
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    heads_per_step = 1
+    for i in range(args.warmup):
+        oracle_sample(p, x64, [i % p.n_h])
+    times = []
+    flops = 0
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        flops += oracle_sample(p, x64, [(args.warmup + i) % p.n_h])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops / total / 1e12
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(p, {"sample": f"{heads_per_step} head(s) of {p.n_h} per step"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"fp64 oracle fwd+bwd of {heads_per_step} head per step (of {p.n_h}), "
+                                   f"batch 0 of the shard; TFLOP/s of that sample's algorithmic flops"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, p: Problem):
+    import ctypes
+
+    import torch
+
+    from mla_attention_sequence_gb300 import build as build_mod
+    from mla_attention_sequence_gb300 import laga
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    build_mod.build()
+    L = laga.lib()
+
+    x = make_inputs(p, SEED + rank)
+    dt = torch.bfloat16 if p.dtype == "bf16" else torch.float32
+    host = {k: torch.from_numpy(v).to(dt).pin_memory() for k, v in x.items()}
+    dinp = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+    torch.cuda.synchronize()
+    buf = laga.alloc_step(p, dinp, args.variant)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        laga.step(buf, args.variant)
+    laga.check(dev)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    L.laga_mla_profile_enable(1)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        laga.step(buf, args.variant)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    nmax = 64 * args.steps
+    names = (ctypes.c_char_p * nmax)()
+    ms = (ctypes.c_float * nmax)()
+    nrec = L.laga_mla_profile_read(ctypes.cast(names, ctypes.POINTER(ctypes.c_char_p)), ms, nmax)
+    L.laga_mla_profile_enable(0)
+    laga.check(dev)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = reduce_max(sum(step_ms), world, dev)
+    per_kernel = {}
+    for i in range(min(nrec, nmax)):
+        n = names[i].decode()
+        per_kernel.setdefault(n, []).append(ms[i])
+
+    # ---- end-to-end through the public API with host buffers
+    out_host = {"out": torch.empty(buf.out.shape, dtype=dt).pin_memory(),
+                "lse": torch.empty(buf.lse.shape, dtype=torch.float32).pin_memory()}
+    for k, v in buf.grads.items():
+        out_host[k] = torch.empty(v.shape, dtype=dt).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e_start[i].record(stream)
+        for k in dinp:
+            dinp[k].copy_(host[k], non_blocking=True)
+        laga.step(buf, args.variant)
+        out_host["out"].copy_(buf.out, non_blocking=True)
+        out_host["lse"].copy_(buf.lse, non_blocking=True)
+        for k, v in buf.grads.items():
+            out_host[k].copy_(v, non_blocking=True)
+        e_end[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)), world, dev)
+
+    flops = p.flops_step()
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops * args.steps / (e2e_ms * 1e-3) / 1e12
+    tokens_s = world * p.B * p.Sq * args.steps / (total_ms * 1e-3)
+    peaks = load_peaks()
+
+    # roofline of the dominant kernel (largest total time)
+    kernel_ms = {k: float(np.mean(v)) for k, v in per_kernel.items()}
+    dom = max(per_kernel, key=lambda k: sum(per_kernel[k])) if per_kernel else None
+    attn_fwd_flops = 2 * p.pairs * p.n_h * (p.d_qk + p.d_v)
+    recon_flops = 2 * p.B * p.skv_eff * p.d_c * p.n_h * (p.d_nope + p.d_v)
+    alg = {"attn_fwd": attn_fwd_flops, "attn_bwd": 2 * attn_fwd_flops, "recon_fwd_gemm": recon_flops,
+           "recon_bwd_dc_gemm": recon_flops, "recon_bwd_dw_gemm": recon_flops}
+    roof = None
+    if dom in alg:
+        achieved = alg[dom] / (kernel_ms[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
+                "flops_per_launch": alg[dom], "ms_per_launch": kernel_ms[dom]}
+    launches_per_step = {"recon_fwd_gemm": 1, "attn_fwd": 1, "bwd_pre": 1, "attn_bwd": 1, "recon_bwd_dc_gemm": 1,
+                         "recon_bwd_dw_gemm": 1, "bwd_post": 2, "simt_fwd": 3, "simt_bwd": 10}
+    gpu_launches = sum(launches_per_step.get(k, 1) * len(v) for k, v in per_kernel.items())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, heads, secs = time_oracle(p, x, budget_s=args.cpu_budget)
+        cpu = {"value": tf, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd of {heads} head(s) (of {p.n_h}) of the same shard, {secs:.1f} s; "
+                         f"TFLOP/s of the sample's algorithmic flops"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(p, {"variant": args.variant}),
+            "tokens_per_s": tokens_s,
+            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "peak_source": peaks["source"],
+            "roofline": roof,
+            "kernels_ms_per_launch": kernel_ms,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": gpu_launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DSV3_LAST_RANK.name, choices=sorted(NAMED))
+    ap.add_argument("--variant", default="auto", choices=["auto", "materialize", "simt"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed steps
+    p = NAMED[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, p)
+    return run_ours(args, p)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -157,6 +157,20 @@ const char* laga_status_string(laga_status status);
 /* Detail of the last error returned on this host thread (static storage). */
 const char* laga_mla_last_error(void);
 
+/* Optional kernel timing. While enabled on the calling host thread, each step
+ * that laga_mla_fwd / laga_mla_bwd launch (one kernel, or a short group of
+ * memory-bound kernels named after their role) is bracketed by two CUDA
+ * events recorded on the caller's stream. Enabling (or
+ * disabling) clears earlier records. The events are created on first use and
+ * reused; nothing is recorded while disabled (the default). */
+laga_status laga_mla_profile_enable(int enable);
+
+/* Waits for the recorded events and writes, for up to `max` launches in launch
+ * order, the kernel's name (static string) and its elapsed time in ms.
+ * Returns the number of launches recorded since the last enable (which may
+ * exceed `max`), or -1 if an event query fails. */
+int laga_mla_profile_read(const char** names, float* ms, int max);
+
 /* Library ABI version: major*10000 + minor*100 + patch. */
 int laga_mla_version(void);
 

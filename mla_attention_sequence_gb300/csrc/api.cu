@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 namespace laga {
 
@@ -35,6 +36,49 @@ laga_status from_launch(const LaunchResult& r) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- opt-in kernel timing: one event pair per launch, events pooled per thread
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<const char*> names;
+  size_t used = 0;  // events handed out since the last enable
+};
+thread_local Profiler t_prof;
+
+cudaEvent_t prof_event() {
+  Profiler& P = t_prof;
+  if (P.used == P.pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    P.pool.push_back(e);
+  }
+  return P.pool[P.used++];
+}
+
+// Records the start event of a launch named `name` (no-op when disabled).
+void prof_begin(const char* name, cudaStream_t s) {
+  if (!t_prof.on) return;
+  cudaEvent_t e = prof_event();
+  if (e) cudaEventRecord(e, s);
+  t_prof.names.push_back(e ? name : nullptr);
+}
+
+void prof_end(cudaStream_t s) {
+  if (!t_prof.on) return;
+  if (!t_prof.names.empty() && t_prof.names.back() == nullptr) return;
+  cudaEvent_t e = prof_event();
+  if (e) cudaEventRecord(e, s);
+}
+
+// Run one launcher between two profiling marks.
+template <class F>
+LaunchResult timed(const char* name, cudaStream_t s, F&& f) {
+  prof_begin(name, s);
+  LaunchResult r = f();
+  prof_end(s);
+  return r;
+}
 
 enum class Path { Invalid, Simt, TensorCore, TensorCoreFused };
 
@@ -197,14 +241,20 @@ laga_status laga_mla_fwd(const laga_mla_desc* desc, const void* q, const void* c
   const size_t need = path == Path::Simt ? simt_fwd_workspace(d) : tc_fwd_workspace(d);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return fail(LAGA_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small%s");
-  if (path == Path::Simt) return from_launch(simt_fwd(d, bf, q, c_kv, k_rope, W_UK, W_UV, out, lse, workspace, s));
+  if (path == Path::Simt)
+    return from_launch(
+        timed("simt_fwd", s, [&] { return simt_fwd(d, bf, q, c_kv, k_rope, W_UK, W_UV, out, lse, workspace, s); }));
   bf16* k_ws = static_cast<bf16*>(workspace);
   bf16* v_ws = k_ws + static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 128;
-  LaunchResult r = tc_recon_fwd(d, static_cast<const bf16*>(c_kv), static_cast<const bf16*>(W_UK),
-                                static_cast<const bf16*>(W_UV), k_ws, v_ws, d.skv_pad, s);
+  LaunchResult r = timed("recon_fwd_gemm", s, [&] {
+    return tc_recon_fwd(d, static_cast<const bf16*>(c_kv), static_cast<const bf16*>(W_UK),
+                        static_cast<const bf16*>(W_UV), k_ws, v_ws, d.skv_pad, s);
+  });
   if (!r.ok()) return from_launch(r);
-  return from_launch(tc_attn_fwd(d, static_cast<const bf16*>(q), k_ws, v_ws, static_cast<const bf16*>(k_rope),
-                                 static_cast<bf16*>(out), lse, s));
+  return from_launch(timed("attn_fwd", s, [&] {
+    return tc_attn_fwd(d, static_cast<const bf16*>(q), k_ws, v_ws, static_cast<const bf16*>(k_rope),
+                       static_cast<bf16*>(out), lse, s);
+  }));
 }
 
 laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
@@ -226,18 +276,26 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(LAGA_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small%s");
   if (path == Path::Simt)
-    return from_launch(simt_bwd(d, bf, q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, dq, dc_kv, dk_rope, dW_UK, dW_UV,
-                                workspace, s));
+    return from_launch(timed("simt_bwd", s, [&] {
+      return simt_bwd(d, bf, q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, dq, dc_kv, dk_rope, dW_UK, dW_UV,
+                      workspace, s);
+    }));
   BwdWorkspace w = tc_bwd_carve(d, workspace);
   auto cb = [](const void* p) { return static_cast<const bf16*>(p); };
-  LaunchResult r = tc_recon_fwd(d, cb(c_kv), cb(W_UK), cb(W_UV), w.k_ws, w.v_ws, d.skv_pad, s);
-  if (r.ok()) r = tc_bwd_pre(d, cb(out), cb(dout), lse, w, s);
-  if (r.ok()) r = tc_attn_bwd(d, cb(q), cb(k_rope), cb(dout), w, s);
+  LaunchResult r = timed("recon_fwd_gemm", s,
+                         [&] { return tc_recon_fwd(d, cb(c_kv), cb(W_UK), cb(W_UV), w.k_ws, w.v_ws, d.skv_pad, s); });
+  if (r.ok()) r = timed("bwd_pre", s, [&] { return tc_bwd_pre(d, cb(out), cb(dout), lse, w, s); });
+  if (r.ok()) r = timed("attn_bwd", s, [&] { return tc_attn_bwd(d, cb(q), cb(k_rope), cb(dout), w, s); });
   if (r.ok())
-    r = tc_recon_bwd_dc(d, w.dk_ws, w.dv_ws, cb(W_UK), cb(W_UV), static_cast<bf16*>(dc_kv), s);
+    r = timed("recon_bwd_dc_gemm", s, [&] {
+      return tc_recon_bwd_dc(d, w.dk_ws, w.dv_ws, cb(W_UK), cb(W_UV), static_cast<bf16*>(dc_kv), s);
+    });
   if (r.ok())
-    r = tc_recon_bwd_dw(d, cb(c_kv), w.dk_ws, w.dv_ws, static_cast<bf16*>(dW_UK), static_cast<bf16*>(dW_UV), s);
-  if (r.ok()) r = tc_bwd_post(d, w, static_cast<bf16*>(dq), static_cast<bf16*>(dk_rope), s);
+    r = timed("recon_bwd_dw_gemm", s, [&] {
+      return tc_recon_bwd_dw(d, cb(c_kv), w.dk_ws, w.dv_ws, static_cast<bf16*>(dW_UK), static_cast<bf16*>(dW_UV), s);
+    });
+  if (r.ok())
+    r = timed("bwd_post", s, [&] { return tc_bwd_post(d, w, static_cast<bf16*>(dq), static_cast<bf16*>(dk_rope), s); });
   if (r.ok() && d.skv_pad < d.S) {
     // Latent rows beyond the padded visible prefix get zero gradient.
     r.err = cudaMemset2DAsync(static_cast<bf16*>(dc_kv) + static_cast<size_t>(d.skv_pad) * d.d_c,
@@ -330,6 +388,31 @@ const char* laga_status_string(laga_status status) {
 }
 
 const char* laga_mla_last_error(void) { return t_last_error; }
+
+laga_status laga_mla_profile_enable(int enable) {
+  t_prof.on = enable != 0;
+  t_prof.used = 0;
+  t_prof.names.clear();
+  return LAGA_OK;
+}
+
+int laga_mla_profile_read(const char** names, float* ms, int max) {
+  const Profiler& P = t_prof;
+  const int n = static_cast<int>(P.names.size());
+  int out = 0;
+  for (int i = 0; i < n && out < max; ++i) {
+    if (P.names[i] == nullptr) continue;
+    if (2 * static_cast<size_t>(i) + 1 >= P.used) break;
+    cudaEvent_t a = P.pool[2 * i], b = P.pool[2 * i + 1];
+    if (cudaEventSynchronize(b) != cudaSuccess) return -1;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, a, b) != cudaSuccess) return -1;
+    if (names) names[out] = P.names[i];
+    if (ms) ms[out] = t;
+    ++out;
+  }
+  return n;
+}
 
 int laga_mla_version(void) { return 100; }
 
