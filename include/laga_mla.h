@@ -146,6 +146,29 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
 laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
                                  const void* W_UV, void* k_nope, void* v, laga_stream_t stream);
 
+/* Largest workspace, in bytes, that laga_mla_fwd_noalloc can stand in for. */
+#define LAGA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* Forward for callers that cannot allocate device memory, and so have no
+ * workspace to pass: a plug-in whose host framework owns all device memory
+ * through its own pool, a runtime with a fixed memory budget, a C caller
+ * without an allocator. Same arguments and results as laga_mla_fwd minus the
+ * workspace; the caller still passes every input and output. The paper has no
+ * counterpart of this entry point: it exists for those callers only.
+ *
+ * The forward's scratch (the per-head K_nope and V) lives in one static device
+ * array of LAGA_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits. Problems whose laga_mla_fwd_workspace_size exceeds
+ * it return LAGA_ERR_WORKSPACE (laga_mla_last_error says by how much). The
+ * first call on each device looks up the array's device address (set-up done
+ * once per device, with that device current); make that first call before any
+ * stream capture. Every call on a device shares the array, which keeps the last
+ * call's contents; calls whose kernels overlap on the GPU race on it, so
+ * serialise them. Allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine. */
+laga_status laga_mla_fwd_noalloc(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
+                                 const void* W_UK, const void* W_UV, void* out, float* lse, laga_stream_t stream);
+
 /* Synchronises the stream, then reads and clears this device's status word.
  * Returns LAGA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
  * check, LAGA_ERR_CUDA if the stream reports an error, else LAGA_OK. */

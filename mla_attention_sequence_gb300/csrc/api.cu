@@ -169,6 +169,8 @@ CuTensorMapEncodeTiled encode_fn() {
 
 }  // namespace
 
+void set_last_error(const char* msg) { std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
+
 int* device_status_ptr() {
   static int* ptrs[64] = {};
   static std::mutex mu;

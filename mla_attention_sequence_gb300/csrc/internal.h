@@ -33,6 +33,9 @@ struct LaunchResult {
 // nullptr if it cannot be resolved.
 int* device_status_ptr();
 
+// Sets the message laga_mla_last_error returns on this host thread.
+void set_last_error(const char* msg);
+
 // ---- tensor-map helper (driver entry point resolved once through the runtime)
 CUresult make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                    const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
