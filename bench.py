@@ -311,7 +311,11 @@ def run_ours(args, p: Problem):
     dom = max(per_kernel, key=lambda k: sum(per_kernel[k])) if per_kernel else None
     attn_fwd_flops = 2 * p.pairs * p.n_h * (p.d_qk + p.d_v)
     recon_flops = 2 * p.B * p.skv_eff * p.d_c * p.n_h * (p.d_nope + p.d_v)
-    alg = {"attn_fwd": attn_fwd_flops, "attn_bwd": 2 * attn_fwd_flops, "recon_fwd_gemm": recon_flops,
+    # backward attention = 2 x forward, split by the products each kernel owns:
+    # dK/dV kernel dV + dP + dK (128 + 128 + 192 per pair and head), dq kernel dQ (192)
+    unit = 2 * p.pairs * p.n_h
+    alg = {"attn_fwd": attn_fwd_flops, "attn_bwd_dkdv": unit * (p.d_v + p.d_v + p.d_qk),
+           "attn_bwd_dq": unit * p.d_qk, "recon_fwd_gemm": recon_flops,
            "recon_bwd_dc_gemm": recon_flops, "recon_bwd_dw_gemm": recon_flops}
     roof = None
     if dom in alg:
@@ -321,8 +325,7 @@ def run_ours(args, p: Problem):
                 "frac": achieved / peak, "traffic": None,
                 "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
                 "flops_per_launch": alg[dom], "ms_per_launch": kernel_ms[dom]}
-    launches_per_step = {"recon_fwd_gemm": 1, "attn_fwd": 1, "bwd_pre": 1, "attn_bwd": 1, "recon_bwd_dc_gemm": 1,
-                         "recon_bwd_dw_gemm": 1, "bwd_post": 2, "simt_fwd": 3, "simt_bwd": 10}
+    launches_per_step = {"simt_fwd": 3, "simt_bwd": 10}  # every other timed step is one kernel
     gpu_launches = sum(launches_per_step.get(k, 1) * len(v) for k, v in per_kernel.items())
 
     cpu = None

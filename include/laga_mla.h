@@ -53,9 +53,8 @@
  *    status word that laga_mla_check reads. No call aborts the process.
  *  - Threads: calls are re-entrant as long as concurrent calls use disjoint
  *    workspaces and outputs.
- *  - Reproducibility: the backward adds per-key-tile contributions to dq with
- *    fp32 atomics, so dq may differ in the last bits between runs; every other
- *    output is produced in a fixed order.
+ *  - Reproducibility: no kernel uses atomics; every output is produced in a
+ *    fixed order, so repeated calls give bitwise-identical results.
  *
  * Supported problems
  * ------------------

@@ -287,7 +287,11 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
   LaunchResult r = timed("recon_fwd_gemm", s,
                          [&] { return tc_recon_fwd(d, cb(c_kv), cb(W_UK), cb(W_UV), w.k_ws, w.v_ws, d.skv_pad, s); });
   if (r.ok()) r = timed("bwd_pre", s, [&] { return tc_bwd_pre(d, cb(out), cb(dout), lse, w, s); });
-  if (r.ok()) r = timed("attn_bwd", s, [&] { return tc_attn_bwd(d, cb(q), cb(k_rope), cb(dout), w, s); });
+  if (r.ok())
+    r = timed("attn_bwd_dkdv", s, [&] { return tc_attn_bwd_dkdv(d, cb(q), cb(k_rope), cb(dout), w, s); });
+  if (r.ok())
+    r = timed("attn_bwd_dq", s,
+              [&] { return tc_attn_bwd_dq(d, cb(q), cb(k_rope), cb(dout), w, static_cast<bf16*>(dq), s); });
   if (r.ok())
     r = timed("recon_bwd_dc_gemm", s, [&] {
       return tc_recon_bwd_dc(d, w.dk_ws, w.dv_ws, cb(W_UK), cb(W_UV), static_cast<bf16*>(dc_kv), s);
@@ -297,7 +301,7 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
       return tc_recon_bwd_dw(d, cb(c_kv), w.dk_ws, w.dv_ws, static_cast<bf16*>(dW_UK), static_cast<bf16*>(dW_UV), s);
     });
   if (r.ok())
-    r = timed("bwd_post", s, [&] { return tc_bwd_post(d, w, static_cast<bf16*>(dq), static_cast<bf16*>(dk_rope), s); });
+    r = timed("bwd_post", s, [&] { return tc_bwd_post(d, w, static_cast<bf16*>(dk_rope), s); });
   if (r.ok() && d.skv_pad < d.S) {
     // Latent rows beyond the padded visible prefix get zero gradient.
     r.err = cudaMemset2DAsync(static_cast<bf16*>(dc_kv) + static_cast<size_t>(d.skv_pad) * d.d_c,

@@ -1,0 +1,427 @@
+// Attention backward, key/value side: dV, dK_nope and each head's RoPE-key
+// gradient, on the tensor cores (d_qk = 128 + 64, d_v = 128, bf16 operands,
+// fp32 accumulation).
+//
+// One CTA per (128-row key tile, head, batch element); it walks the 64-row
+// query tiles that can see its keys. Keys sit on the TMEM lanes:
+//   S^T  = K Q^T          P^T  = exp(S^T * scale - lse)
+//   dP^T = V dO^T         dS^T = P^T o (dP^T - D)
+//   dV  += P^T dO         dK  += dS^T Q        (scale applied once at the end)
+// P^T and dS^T are written back into TMEM as packed bf16 over S^T / dP^T and
+// feed the dV / dK products as the A operand straight from TMEM, so they never
+// touch shared memory. dK covers all 192 head dims in one N = 192 product: the
+// first 128 columns are dK_nope, the last 64 this head's RoPE-key gradient.
+//
+// Warp roles (192 threads):
+//   warp 0      lane 0: TMA for the key/value tile, then Q, dO, lse, D tiles
+//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
+//   warps 2..5  one key row per thread: P^T, dS^T, and the final epilogue
+// TMEM columns: dV [0,128), dK [128,320), S^T/P^T x2 [320,448), dP^T/dS^T [448,512).
+// MMA order S(0) dP(0) S(1) | dV(i) dK(i) dP(i+1) S(i+2) | ... keeps the next
+// query tile's products queued behind the current one's.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace laga {
+namespace {
+
+constexpr int BKV = 128;
+constexpr int BQ = 64;
+constexpr int NSTAGE = 3;
+constexpr int KBOX = 16384;  // [128 rows][64] bf16
+constexpr int QBOX = 8192;   // [64 rows][64] bf16
+constexpr int K_BYTES = 3 * KBOX;
+constexpr int V_BYTES = 2 * KBOX;
+constexpr int Q_BYTES = 3 * QBOX;
+constexpr int DO_BYTES = 2 * QBOX;
+constexpr int ROWV_BYTES = BQ * 4;
+constexpr int STAGE_BYTES = Q_BYTES + DO_BYTES;  // 40 KB, 1024-aligned
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + K_BYTES;
+constexpr int OFF_STAGE = OFF_V + V_BYTES;
+constexpr int OFF_ROWV = OFF_STAGE + NSTAGE * STAGE_BYTES;
+constexpr int OFF_BARS = OFF_ROWV + NSTAGE * 2 * ROWV_BYTES;
+constexpr int SMEM_BYTES = OFF_BARS + 256 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 320, COL_DP = 448;
+constexpr uint32_t IDESC_ST = idesc_bf16(128, 64, false, false);   // S^T, dP^T
+constexpr uint32_t IDESC_DV = idesc_bf16(128, 128, false, true);   // dV (A from TMEM)
+constexpr uint32_t IDESC_DK = idesc_bf16(128, 192, false, true);   // dK (A from TMEM)
+
+struct Params {
+  int* status;
+  int Sq, S, n_h, q_offset, causal, skv_pad, sq_pad;
+  float scale, scale_log2;
+  const float* lse2;
+  const float* delta;
+  bf16* dk_ws;
+  bf16* dv_ws;
+  float* dkr_ws;
+};
+
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                         const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
+                         const __grid_constant__ CUtensorMap mdO, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;   // [NSTAGE]
+  uint64_t* q_empty = bars + 4;  // [NSTAGE]
+  uint64_t* s_full = bars + 7;   // [2]
+  uint64_t* dp_full = bars + 9;
+  // P^T of step i+1 can be ready before the MMA thread has seen step i's, so
+  // p_full alternates between two barriers (one phase of each per two steps).
+  uint64_t* p_full = bars + 10;  // [2]
+  uint64_t* ds_full = bars + 12;
+  uint64_t* acc_done = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int kv0 = blockIdx.x * BKV;  // low key tiles see the most queries: launched first
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int first_qt = p.causal ? max(0, kv0 - p.q_offset) / BQ : 0;
+  const int n_qt = (p.Sq + BQ - 1) / BQ - first_qt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(dp_full, 1);
+    mbar_init(&p_full[0], 4);
+    mbar_init(&p_full[1], 4);
+    mbar_init(ds_full, 4);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mR);
+      tma_prefetch_desc(&mV);
+      tma_prefetch_desc(&mdO);
+      mbar_arrive_expect_tx(kv_full, K_BYTES + V_BYTES);
+      const int krow = b * p.skv_pad + kv0;
+      tma_load_2d(smem + OFF_K, &mK, kv_full, h * 128, krow);
+      tma_load_2d(smem + OFF_K + KBOX, &mK, kv_full, h * 128 + 64, krow);
+      tma_load_3d(smem + OFF_K + 2 * KBOX, &mR, kv_full, 0, kv0, b);
+      tma_load_2d(smem + OFF_V, &mV, kv_full, h * 128, krow);
+      tma_load_2d(smem + OFF_V + KBOX, &mV, kv_full, h * 128 + 64, krow);
+      int i = 0;
+      for (; i < n_qt; ++i) {
+        const int s = i % NSTAGE;
+        if (!mbar_wait_or_abort(&q_empty[s], ((i / NSTAGE) & 1) ^ 1, abort_flag, 51)) break;
+        const int q0 = (first_qt + i) * BQ;
+        uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
+        float* rows = reinterpret_cast<float*>(smem + OFF_ROWV) + s * 2 * BQ;
+        mbar_arrive_expect_tx(&q_full[s], STAGE_BYTES + 2 * ROWV_BYTES);
+        tma_load_3d(st, &mQ, &q_full[s], h * 192, q0, b);
+        tma_load_3d(st + QBOX, &mQ, &q_full[s], h * 192 + 64, q0, b);
+        tma_load_3d(st + 2 * QBOX, &mQ, &q_full[s], h * 192 + 128, q0, b);
+        tma_load_3d(st + Q_BYTES, &mdO, &q_full[s], h * 128, q0, b);
+        tma_load_3d(st + Q_BYTES + QBOX, &mdO, &q_full[s], h * 128 + 64, q0, b);
+        const long long roff = (static_cast<long long>(b) * p.n_h + h) * p.sq_pad + q0;
+        bulk_load(rows, p.lse2 + roff, ROWV_BYTES, &q_full[s]);
+        bulk_load(rows + BQ, p.delta + roff, ROWV_BYTES, &q_full[s]);
+      }
+      if (i < n_qt) {
+        mbar_drain(kv_full, 0);
+        for (int k = i - NSTAGE < 0 ? 0 : i - NSTAGE; k < i; ++k)
+          mbar_drain(&q_full[k % NSTAGE], (k / NSTAGE) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait_or_abort(kv_full, 0, abort_flag, 52);
+      bool issued = false;
+      tc_fence_after();
+      const uint32_t k_base = smem_u32(smem + OFF_K);
+      const uint32_t v_base = smem_u32(smem + OFF_V);
+      auto stage = [&](int i) { return smem_u32(smem + OFF_STAGE + (i % NSTAGE) * STAGE_BYTES); };
+      auto wait_q = [&](int i) {
+        return mbar_wait_or_abort(&q_full[i % NSTAGE], (i / NSTAGE) & 1, abort_flag, 53);
+      };
+      auto issue_s = [&](int i) {  // S^T(i) = K Q_i^T
+        const uint32_t q_base = stage(i);
+        const uint32_t d = tmem + COL_S + 64u * (i & 1);
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint32_t c = kk >> 2, k = kk & 3;
+          mma_ss(d, sdesc_sw128(k_base + c * KBOX + k * 32, 16, 1024),
+                 sdesc_sw128(q_base + c * QBOX + k * 32, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[i & 1]);
+      };
+      auto issue_dp = [&](int i) {  // dP^T(i) = V dO_i^T
+        const uint32_t do_base = stage(i) + Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t c = kk >> 2, k = kk & 3;
+          mma_ss(tmem + COL_DP, sdesc_sw128(v_base + c * KBOX + k * 32, 16, 1024),
+                 sdesc_sw128(do_base + c * QBOX + k * 32, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(dp_full);
+      };
+      if (ok && n_qt > 0) {
+        ok = wait_q(0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
+          issued = true;
+        }
+        if (ok && n_qt > 1) {
+          ok = wait_q(1);
+          if (ok) {
+            tc_fence_after();
+            issue_s(1);
+          }
+        }
+      }
+      for (int i = 0; i < n_qt && ok; ++i) {
+        const uint32_t q_base = stage(i);
+        const uint32_t do_base = q_base + Q_BYTES;
+        if (!mbar_wait_or_abort(&p_full[i & 1], (i >> 1) & 1, abort_flag, 54)) { ok = false; break; }
+        tc_fence_after();
+        // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
+        const uint32_t pt = tmem + COL_S + 64u * (i & 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(tmem + COL_DV, pt + 8 * k, sdesc_sw128(do_base + k * 2048, QBOX, 1024), IDESC_DV,
+                 (i > 0 || k > 0) ? 1u : 0u);
+        if (!mbar_wait_or_abort(ds_full, i & 1, abort_flag, 55)) { ok = false; break; }
+        tc_fence_after();
+        // dK += dS^T Q_i : all 192 head dims in one product
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(tmem + COL_DK, tmem + COL_DP + 8 * k, sdesc_sw128(q_base + k * 2048, QBOX, 1024), IDESC_DK,
+                 (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&q_empty[i % NSTAGE]);
+        if (i + 1 < n_qt) issue_dp(i + 1);
+        if (i + 2 < n_qt) {
+          if (!wait_q(i + 2)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(i + 2);
+        }
+      }
+      if (ok) {
+        mma_commit(acc_done);
+      } else if (issued) {
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ key-row warps
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int kv = kv0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // local queries i >= q_min see this key (causal); non-causal: key must exist
+    const int q_min = p.causal ? kv - p.q_offset : 0;
+    const bool key_exists = kv < p.S;
+    bool ok = true;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+      bool w = true;
+      if (lane == 0) w = mbar_wait_or_abort(bar, parity, abort_flag, where);
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    for (int i = 0; i < n_qt; ++i) {
+      const int s = i % NSTAGE;
+      const int q0 = (first_qt + i) * BQ;
+      if (!warp_wait(&q_full[s], (i / NSTAGE) & 1, 61)) { ok = false; break; }
+      if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, 62)) { ok = false; break; }
+      tc_fence_after();
+      const float* rows = reinterpret_cast<const float*>(smem + OFF_ROWV) + s * 2 * BQ;
+      const uint32_t s_addr = tmem + COL_S + 64u * (i & 1) + lane_off;
+      float pr[64];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(s_addr + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int qi = c * 32 + k;
+            const bool vis = p.causal ? (q0 + qi >= q_min) : key_exists;
+            const float x = fmaf(__uint_as_float(u[k]), p.scale_log2, -rows[qi]);
+            pr[qi] = vis ? ex2_approx(x) : 0.f;
+          }
+        }
+      }
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+        tmem_st32(s_addr, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      if (!warp_wait(dp_full, i & 1, 63)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t dp_addr = tmem + COL_DP + lane_off;
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(dp_addr + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int qi = c * 32 + k;
+            pr[qi] = pr[qi] * (__uint_as_float(u[k]) - rows[BQ + qi]);
+          }
+        }
+      }
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+        tmem_st32(dp_addr, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (ok && warp_wait(acc_done, 0, 64)) {
+      tc_fence_after();
+      const long long row = static_cast<long long>(b) * p.skv_pad + kv;
+      const long long ncol = static_cast<long long>(p.n_h) * 128;
+      bf16* dv = p.dv_ws + row * ncol + h * 128;
+      bf16* dk = p.dk_ws + row * ncol + h * 128;
+      float* dkr = p.dkr_ws + (row * p.n_h + h) * 64;
+#pragma unroll 1
+      for (int c = 0; c < 10; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + c * 32, u);  // dV cols 0..127, dK cols 128..319
+        tmem_wait_ld();
+        if (c < 8) {
+          const float sc = c < 4 ? 1.f : p.scale;
+          bf16* dst = c < 4 ? dv + c * 32 : dk + (c - 4) * 32;
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * sc, __uint_as_float(u[8 * v + 1]) * sc);
+            w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * sc, __uint_as_float(u[8 * v + 3]) * sc);
+            w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * sc, __uint_as_float(u[8 * v + 5]) * sc);
+            w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * sc, __uint_as_float(u[8 * v + 7]) * sc);
+            d4[v] = w;
+          }
+        } else {
+          float4* d4 = reinterpret_cast<float4*>(dkr + (c - 8) * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(__uint_as_float(u[4 * v]) * p.scale, __uint_as_float(u[4 * v + 1]) * p.scale,
+                                __uint_as_float(u[4 * v + 2]) * p.scale, __uint_as_float(u[4 * v + 3]) * p.scale);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) publish_abort(abort_flag, p.status);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, const bf16* dout,
+                              const BwdWorkspace& w, cudaStream_t st) {
+  LaunchResult r;
+  CUtensorMap mQ, mK, mR, mV, mdO;
+  const uint32_t qbox[3] = {64, BQ, 1};
+  {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 192;
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
+    r.cu = make_tmap(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 128;
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
+    r.cu = make_tmap(&mdO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dout, dims, strides, qbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t kv_inner = static_cast<uint64_t>(d.n_h) * 128;
+  const uint64_t kv_rows = static_cast<uint64_t>(d.B) * d.skv_pad;
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t dims[2] = {kv_inner, kv_rows};
+    const uint64_t strides[1] = {kv_inner * 2};
+    const uint32_t box[2] = {64, BKV};
+    r.cu = make_tmap(&mK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.k_ws, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r.cu == CUDA_SUCCESS)
+      r.cu = make_tmap(&mV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.v_ws, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(d.S), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(d.S) * 128};
+    const uint32_t box[3] = {64, BKV, 1};
+    r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor maps attention backward (dK, dV)";
+    return r;
+  }
+  Params p{};
+  p.status = device_status_ptr();
+  p.Sq = d.Sq;
+  p.S = d.S;
+  p.n_h = d.n_h;
+  p.q_offset = d.q_offset;
+  p.causal = d.causal ? 1 : 0;
+  p.skv_pad = d.skv_pad;
+  p.sq_pad = d.sq_pad;
+  p.scale = d.scale;
+  p.scale_log2 = d.scale * 1.4426950408889634f;
+  p.lse2 = w.lse2;
+  p.delta = w.delta;
+  p.dk_ws = w.dk_ws;
+  p.dv_ws = w.dv_ws;
+  p.dkr_ws = w.dkr_ws;
+  r.err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (r.err != cudaSuccess) {
+    r.what = "cudaFuncSetAttribute(attn_bwd_dkdv)";
+    return r;
+  }
+  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, d.n_h, d.B), 192, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
+  r.err = cudaGetLastError();
+  if (r.err != cudaSuccess) r.what = "attn_bwd_dkdv_kernel launch";
+  return r;
+}
+
+}  // namespace laga

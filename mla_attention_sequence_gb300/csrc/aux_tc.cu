@@ -1,10 +1,9 @@
 // Workspace layout and the small memory-bound kernels around the tensor-core
 // attention backward:
-//   pre   D_i = dout_i . out_i and lse in the log2 domain, padded per (b, h) row;
-//         dq accumulator cleared
-//   post  dq = scale * accumulated dS K (fp32 -> bf16); dk_rope = sum over
-//         heads of the per-head RoPE-key gradients (the RoPE key is one tensor
-//         shared by every head, so its gradient collects all of them)
+//   pre   D_i = dout_i . out_i and lse in the log2 domain, padded per (b, h) row
+//   post  dk_rope = sum over heads of the per-head RoPE-key gradients (the RoPE
+//         key is one tensor shared by every head, so its gradient collects all
+//         of them)
 #include "internal.h"
 
 namespace laga {
@@ -20,9 +19,8 @@ size_t tc_fwd_workspace(const Dims& d) { return 2 * kv_ws_bytes(d); }
 size_t tc_bwd_workspace(const Dims& d) {
   const size_t kv = kv_ws_bytes(d);
   const size_t dkr = align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 64 * 4, 256);
-  const size_t dq = align_up(static_cast<size_t>(d.B) * d.Sq * d.n_h * 192 * 4, 256);
   const size_t rows = align_up(static_cast<size_t>(d.B) * d.n_h * d.sq_pad * 4, 256);
-  return 4 * kv + dkr + dq + 2 * rows;
+  return 4 * kv + dkr + 2 * rows;
 }
 
 BwdWorkspace tc_bwd_carve(const Dims& d, void* ws) {
@@ -39,8 +37,6 @@ BwdWorkspace tc_bwd_carve(const Dims& d, void* ws) {
   p += kv;
   w.dkr_ws = reinterpret_cast<float*>(p);
   p += align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 64 * 4, 256);
-  w.dq_acc = reinterpret_cast<float*>(p);
-  p += align_up(static_cast<size_t>(d.B) * d.Sq * d.n_h * 192 * 4, 256);
   w.lse2 = reinterpret_cast<float*>(p);
   p += align_up(static_cast<size_t>(d.B) * d.n_h * d.sq_pad * 4, 256);
   w.delta = reinterpret_cast<float*>(p);
@@ -89,19 +85,6 @@ __global__ void bwd_pre_kernel(Dims d, const bf16* __restrict__ out, const bf16*
   }
 }
 
-__global__ void dq_convert_kernel(long long n4, float scale, const float4* __restrict__ acc,
-                                  uint2* __restrict__ dq) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n4) return;
-  const float4 v = acc[i];
-  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * scale, v.y * scale);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * scale, v.w * scale);
-  uint2 o;
-  o.x = *reinterpret_cast<uint32_t*>(&lo);
-  o.y = *reinterpret_cast<uint32_t*>(&hi);
-  dq[i] = o;
-}
-
 // dk_rope[b, j, :] = sum_h dkr[b, j, h, :]; 16 threads x 4 columns per row.
 __global__ void rope_sum_kernel(Dims d, const float* __restrict__ dkr, bf16* __restrict__ dk_rope) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -136,11 +119,6 @@ __global__ void rope_sum_kernel(Dims d, const float* __restrict__ dkr, bf16* __r
 LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const float* lse, const BwdWorkspace& w,
                         cudaStream_t st) {
   LaunchResult r;
-  r.err = cudaMemsetAsync(w.dq_acc, 0, static_cast<size_t>(d.B) * d.Sq * d.n_h * 192 * 4, st);
-  if (r.err != cudaSuccess) {
-    r.what = "clear dq accumulator";
-    return r;
-  }
   const long long rows = static_cast<long long>(d.B) * d.n_h * d.sq_pad;
   bwd_pre_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(d, out, dout, lse, w.lse2, w.delta);
   r.err = cudaGetLastError();
@@ -148,11 +126,8 @@ LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const 
   return r;
 }
 
-LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dq, bf16* dk_rope, cudaStream_t st) {
+LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dk_rope, cudaStream_t st) {
   LaunchResult r;
-  const long long n4 = static_cast<long long>(d.B) * d.Sq * d.n_h * 192 / 4;
-  dq_convert_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(
-      n4, d.scale, reinterpret_cast<const float4*>(w.dq_acc), reinterpret_cast<uint2*>(dq));
   const long long t = static_cast<long long>(d.B) * d.S * 16;
   rope_sum_kernel<<<static_cast<unsigned>((t + 255) / 256), 256, 0, st>>>(d, w.dkr_ws, dk_rope);
   r.err = cudaGetLastError();

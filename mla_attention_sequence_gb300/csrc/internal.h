@@ -79,7 +79,6 @@ struct BwdWorkspace {
   bf16* dk_ws;      // [B][skv_pad][n_h*128]
   bf16* dv_ws;      // [B][skv_pad][n_h*128]
   float* dkr_ws;    // [B][skv_pad][n_h][64]  per-head RoPE-key gradient
-  float* dq_acc;    // [B][Sq][n_h][192]
   float* lse2;      // [B][n_h][sq_pad]  lse * log2(e), +inf on padded rows
   float* delta;     // [B][n_h][sq_pad]  rowsum(dout * out), 0 on padded rows
 };
@@ -87,9 +86,14 @@ BwdWorkspace tc_bwd_carve(const Dims& d, void* ws);
 
 LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const float* lse, const BwdWorkspace& w,
                         cudaStream_t st);
-LaunchResult tc_attn_bwd(const Dims& d, const bf16* q, const bf16* k_rope, const bf16* dout,
-                         const BwdWorkspace& w, cudaStream_t st);
-LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dq, bf16* dk_rope, cudaStream_t st);
+// dV, dK_nope (bf16) and per-head RoPE-key gradients (fp32) into the workspace.
+LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, const bf16* dout,
+                              const BwdWorkspace& w, cudaStream_t st);
+// dq, written once per element from a TMEM accumulator.
+LaunchResult tc_attn_bwd_dq(const Dims& d, const bf16* q, const bf16* k_rope, const bf16* dout,
+                            const BwdWorkspace& w, bf16* dq, cudaStream_t st);
+// dk_rope = sum over heads of the per-head RoPE-key gradients.
+LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dk_rope, cudaStream_t st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

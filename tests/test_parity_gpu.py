@@ -219,8 +219,8 @@ def test_sequence_parallel_shards_on_gpu():
         # same tiles, same order: forward rows are bitwise those of SP=1
         assert torch.equal(g["out"], full["out"][:, r * sh:(r + 1) * sh])
         assert torch.equal(g["lse"], full["lse"][:, :, r * sh:(r + 1) * sh])
-        ref_dq = np64(full["dq"][:, r * sh:(r + 1) * sh])
-        assert np.abs(np64(g["dq"]) - ref_dq).max() <= 1e-2 * np.abs(ref_dq).max()
+        # dq rows come from the same query tiles walking the same key tiles
+        assert torch.equal(g["dq"], full["dq"][:, r * sh:(r + 1) * sh])
         for k in sums:
             sums[k] = sums[k] + np64(g[k])
     for k in sums:
@@ -233,7 +233,6 @@ def test_determinism():
     x = make_inputs(p, seed=14)
     a = run_gpu(p, x)
     b = run_gpu(p, x)
-    for k in ("out", "lse", "dc_kv", "dk_rope", "dW_UK", "dW_UV"):
+    # no atomics anywhere: every output is produced in a fixed order
+    for k in ("out", "lse", "dq", "dc_kv", "dk_rope", "dW_UK", "dW_UV"):
         assert torch.equal(a[k], b[k]), k
-    # dq adds per-key-tile partial sums with fp32 atomics: order may vary
-    assert np.abs(np64(a["dq"]) - np64(b["dq"])).max() <= 1e-2 * np.abs(np64(a["dq"])).max()
