@@ -117,7 +117,19 @@ typedef struct {
   float softmax_scale; /* <= 0 selects 1/sqrt(d_nope + d_rope) */
   int32_t dtype;     /* laga_dtype */
   int32_t variant;   /* laga_variant */
+  int32_t flags;     /* bitwise OR of laga_flags (0 = none) */
 } laga_mla_desc;
+
+/* Descriptor flags.
+ *  LAGA_FLAG_REUSE_KV (laga_mla_bwd): the workspace passed to laga_mla_bwd is
+ *    the one laga_mla_fwd used for the same inputs and descriptor, and its
+ *    first laga_mla_fwd_workspace_size bytes still hold the per-head K_nope
+ *    and V the forward rebuilt there. The backward then reads them instead of
+ *    rebuilding them. The backward workspace layout starts with the forward
+ *    one, so one buffer of laga_mla_bwd_workspace_size bytes serves both
+ *    calls. Keeping K/V alive between the calls is the memory profile of the
+ *    explicit MLA form, which stores per-head K and V for its backward. */
+typedef enum { LAGA_FLAG_REUSE_KV = 1 } laga_flags;
 
 /* Bytes of device workspace laga_mla_fwd / laga_mla_bwd need for this
  * problem (0 if the descriptor is invalid or unsupported). The workspace must

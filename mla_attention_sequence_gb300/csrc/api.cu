@@ -105,6 +105,10 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
     *st = fail(LAGA_ERR_UNSUPPORTED, "problem too large%s");
     return Path::Invalid;
   }
+  if ((x.flags & ~static_cast<int32_t>(LAGA_FLAG_REUSE_KV)) != 0) {
+    *st = fail(LAGA_ERR_INVALID_ARG, "unknown bits in flags%s");
+    return Path::Invalid;
+  }
   if (x.dtype != LAGA_DTYPE_F32 && x.dtype != LAGA_DTYPE_BF16) {
     *st = fail(LAGA_ERR_UNSUPPORTED, "dtype must be LAGA_DTYPE_F32 or LAGA_DTYPE_BF16%s");
     return Path::Invalid;
@@ -280,12 +284,14 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
   if (path == Path::Simt)
     return from_launch(timed("simt_bwd", s, [&] {
       return simt_bwd(d, bf, q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, dq, dc_kv, dk_rope, dW_UK, dW_UV,
-                      workspace, s);
+                      workspace, (desc->flags & LAGA_FLAG_REUSE_KV) != 0, s);
     }));
   BwdWorkspace w = tc_bwd_carve(d, workspace);
   auto cb = [](const void* p) { return static_cast<const bf16*>(p); };
-  LaunchResult r = timed("recon_fwd_gemm", s,
-                         [&] { return tc_recon_fwd(d, cb(c_kv), cb(W_UK), cb(W_UV), w.k_ws, w.v_ws, d.skv_pad, s); });
+  LaunchResult r;
+  if (!(desc->flags & LAGA_FLAG_REUSE_KV))
+    r = timed("recon_fwd_gemm", s,
+              [&] { return tc_recon_fwd(d, cb(c_kv), cb(W_UK), cb(W_UV), w.k_ws, w.v_ws, d.skv_pad, s); });
   if (r.ok()) r = timed("bwd_pre", s, [&] { return tc_bwd_pre(d, cb(out), cb(dout), lse, w, s); });
   if (r.ok())
     r = timed("attn_bwd_dkdv", s, [&] { return tc_attn_bwd_dkdv(d, cb(q), cb(k_rope), cb(dout), w, s); });

@@ -12,10 +12,11 @@
 // touch shared memory. dK covers all 192 head dims in one N = 192 product: the
 // first 128 columns are dK_nope, the last 64 this head's RoPE-key gradient.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      lane 0: TMA for the key/value tile, then Q, dO, lse, D tiles
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
-//   warps 2..5  one key row per thread: P^T, dS^T, and the final epilogue
+//   warps 2..9  two warpgroups; each thread owns one key row (TMEM lane) and
+//               half of the 64 query columns: P^T, dS^T, and half the epilogue
 // TMEM columns: dV [0,128), dK [128,320), S^T/P^T x2 [320,448), dP^T/dS^T [448,512).
 // MMA order S(0) dP(0) S(1) | dV(i) dK(i) dP(i+1) S(i+2) | ... keeps the next
 // query tile's products queued behind the current one's.
@@ -47,6 +48,12 @@ constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 320, COL_DP = 448;
 constexpr uint32_t IDESC_ST = idesc_bf16(128, 64, false, false);   // S^T, dP^T
 constexpr uint32_t IDESC_DV = idesc_bf16(128, 128, false, true);   // dV (A from TMEM)
 constexpr uint32_t IDESC_DK = idesc_bf16(128, 192, false, true);   // dK (A from TMEM)
+constexpr int NTHREADS = 320;
+constexpr uint32_t SOFTMAX_WARPS = 8;
+
+// TMEM column of packed bf16 chunk k (16 queries) of a 64-query tile: the two
+// warpgroups pack their halves at columns [0,16) and [32,48).
+__device__ __forceinline__ uint32_t packed_col(int k) { return 8u * k + 16u * (k >> 1); }
 
 struct Params {
   int* status;
@@ -59,7 +66,7 @@ struct Params {
   float* dkr_ws;
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                          const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
                          const __grid_constant__ CUtensorMap mdO, const Params p) {
@@ -98,9 +105,9 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(dp_full, 1);
-    mbar_init(&p_full[0], 4);
-    mbar_init(&p_full[1], 4);
-    mbar_init(ds_full, 4);
+    mbar_init(&p_full[0], SOFTMAX_WARPS);
+    mbar_init(&p_full[1], SOFTMAX_WARPS);
+    mbar_init(ds_full, SOFTMAX_WARPS);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -209,14 +216,14 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t pt = tmem + COL_S + 64u * (i & 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + COL_DV, pt + 8 * k, sdesc_sw128(do_base + k * 2048, QBOX, 1024), IDESC_DV,
+          mma_ts(tmem + COL_DV, pt + packed_col(k), sdesc_sw128(do_base + k * 2048, QBOX, 1024), IDESC_DV,
                  (i > 0 || k > 0) ? 1u : 0u);
         if (!mbar_wait_or_abort(ds_full, i & 1, abort_flag, 55)) { ok = false; break; }
         tc_fence_after();
         // dK += dS^T Q_i : all 192 head dims in one product
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + COL_DK, tmem + COL_DP + 8 * k, sdesc_sw128(q_base + k * 2048, QBOX, 1024), IDESC_DK,
+          mma_ts(tmem + COL_DK, tmem + COL_DP + packed_col(k), sdesc_sw128(q_base + k * 2048, QBOX, 1024), IDESC_DK,
                  (i > 0 || k > 0) ? 1u : 0u);
         mma_commit(&q_empty[i % NSTAGE]);
         if (i + 1 < n_qt) issue_dp(i + 1);
@@ -236,12 +243,12 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------ key-row warps
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // warpgroup: query columns [32*half, 32*half + 32)
     const int r = quarter * 32 + lane;
     const int kv = kv0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // local queries i >= q_min see this key (causal); non-causal: key must exist
-    const int q_min = p.causal ? kv - p.q_offset : 0;
-    const bool key_exists = kv < p.S;
+    // local queries i >= q_min see this key (causal); non-causal: the key must exist
+    const int q_min = p.causal ? kv - p.q_offset : (kv < p.S ? 0 : 0x7fffffff);
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
       bool w = true;
@@ -250,33 +257,34 @@ __global__ void __launch_bounds__(192, 1)
     };
     for (int i = 0; i < n_qt; ++i) {
       const int s = i % NSTAGE;
-      const int q0 = (first_qt + i) * BQ;
+      const int qc = (first_qt + i) * BQ + 32 * half;  // this thread's first query column
       if (!warp_wait(&q_full[s], (i / NSTAGE) & 1, 61)) { ok = false; break; }
       if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, 62)) { ok = false; break; }
       tc_fence_after();
-      const float* rows = reinterpret_cast<const float*>(smem + OFF_ROWV) + s * 2 * BQ;
+      const float* lse = reinterpret_cast<const float*>(smem + OFF_ROWV) + s * 2 * BQ + 32 * half;
+      const float* dlt = lse + BQ;
       const uint32_t s_addr = tmem + COL_S + 64u * (i & 1) + lane_off;
-      float pr[64];
+      float pr[32];
       {
         uint32_t u[32];
+        tmem_ld32(s_addr + 32 * half, u);
+        tmem_wait_ld();
+        if (qc >= q_min) {  // every query of the half-tile sees this key
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(s_addr + c * 32, u);
-          tmem_wait_ld();
+          for (int k = 0; k < 32; ++k) pr[k] = ex2_approx(fmaf(__uint_as_float(u[k]), p.scale_log2, -lse[k]));
+        } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int qi = c * 32 + k;
-            const bool vis = p.causal ? (q0 + qi >= q_min) : key_exists;
-            const float x = fmaf(__uint_as_float(u[k]), p.scale_log2, -rows[qi]);
-            pr[qi] = vis ? ex2_approx(x) : 0.f;
-          }
+          for (int k = 0; k < 32; ++k)
+            pr[k] = qc + k >= q_min ? ex2_approx(fmaf(__uint_as_float(u[k]), p.scale_log2, -lse[k])) : 0.f;
         }
       }
       {
-        uint32_t w[32];
+        uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
-        tmem_st32(s_addr, w);
+        for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+        // P^T packed in place over this half's own score columns (query pair k -> column
+        // 32*half + k), so the other warpgroup's scores are never overwritten unread
+        tmem_st16(s_addr + 32 * half, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -287,22 +295,14 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t dp_addr = tmem + COL_DP + lane_off;
       {
         uint32_t u[32];
+        tmem_ld32(dp_addr + 32 * half, u);
+        tmem_wait_ld();
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(dp_addr + c * 32, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int qi = c * 32 + k;
-            pr[qi] = pr[qi] * (__uint_as_float(u[k]) - rows[BQ + qi]);
-          }
-        }
-      }
-      {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
-        tmem_st32(dp_addr, w);
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(pr[2 * k] * (__uint_as_float(u[2 * k]) - dlt[2 * k]),
+                             pr[2 * k + 1] * (__uint_as_float(u[2 * k + 1]) - dlt[2 * k + 1]));
+        tmem_st16(dp_addr + 32 * half, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -316,10 +316,12 @@ __global__ void __launch_bounds__(192, 1)
       bf16* dv = p.dv_ws + row * ncol + h * 128;
       bf16* dk = p.dk_ws + row * ncol + h * 128;
       float* dkr = p.dkr_ws + (row * p.n_h + h) * 64;
+      // TMEM columns: dV 0..127, dK 128..319 (no-RoPE 128..255, RoPE 256..319);
+      // warpgroup 0 writes chunks 0..4, warpgroup 1 chunks 5..9 (32 columns each)
 #pragma unroll 1
-      for (int c = 0; c < 10; ++c) {
+      for (int c = 5 * half; c < 5 * half + 5; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem + lane_off + c * 32, u);  // dV cols 0..127, dK cols 128..319
+        tmem_ld32(tmem + lane_off + c * 32, u);
         tmem_wait_ld();
         if (c < 8) {
           const float sc = c < 4 ? 1.f : p.scale;
@@ -418,7 +420,7 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
     r.what = "cudaFuncSetAttribute(attn_bwd_dkdv)";
     return r;
   }
-  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, d.n_h, d.B), 192, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
+  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_bwd_dkdv_kernel launch";
   return r;

@@ -12,10 +12,11 @@
 // the forward: S = Q_nope K_nope^T + Q_rope k_rope^T, and dq's last 64 columns
 // come from the k_rope tile.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      lane 0: TMA for Q and dO once, then key tiles; lane 1: value tiles
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
-//   warps 2..5  one query row per thread: P, dS, and the epilogue
+//   warps 2..9  two warpgroups; each thread owns one query row (TMEM lane) and
+//               half of the tile's 64 key columns: P, dS, and half the epilogue
 // TMEM columns: S/dS x2 [0,128), dP x2 [128,256), dq [256,448).
 #include "internal.h"
 #include "ptx.cuh"
@@ -42,6 +43,8 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
 constexpr uint32_t IDESC_DQ = idesc_bf16(128, 192, false, true);
+constexpr int NTHREADS = 320;
+constexpr uint32_t SOFTMAX_WARPS = 8;
 
 struct Params {
   int* status;
@@ -52,12 +55,16 @@ struct Params {
   bf16* dq;
 };
 
+// TMEM column of packed bf16 chunk k (16 keys) of a 64-key tile: the two
+// warpgroups pack their halves at columns [0,16) and [32,48).
+__device__ __forceinline__ uint32_t packed_col(int k) { return 8u * k + 16u * (k >> 1); }
+
 __device__ __forceinline__ int n_kv_tiles(const Params& p, int t) {
   const int last = p.causal ? p.q_offset + min(p.Sq, (t + 1) * BQ) - 1 : p.S - 1;
   return last / BKV + 1;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                        const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
                        const __grid_constant__ CUtensorMap mdO, const Params p) {
@@ -94,7 +101,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&ds_full[i], 4);
+      mbar_init(&ds_full[i], SOFTMAX_WARPS);
     }
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t ds = tmem + COL_S + 64u * (j & 1);
 #pragma unroll
         for (int k = 0; k < BKV / 16; ++k)
-          mma_ts(tmem + COL_DQ, ds + 8 * k, sdesc_sw128(k_base + k * 2048, KBOX, 1024), IDESC_DQ,
+          mma_ts(tmem + COL_DQ, ds + packed_col(k), sdesc_sw128(k_base + k * 2048, KBOX, 1024), IDESC_DQ,
                  (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&k_empty[s]);
       }
@@ -217,12 +224,13 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------ query-row warps
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // warpgroup: key columns [32*half, 32*half + 32)
     const int r = quarter * 32 + lane;
     const int q_row = t * BQ + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int limit = p.causal ? p.q_offset + q_row : p.S - 1;  // last visible key
     const long long roff = (static_cast<long long>(b) * p.n_h + h) * p.sq_pad + q_row;
-    const float lse2 = p.lse2[roff];   // +inf on padded rows: P = 0 there
+    const float lse2 = p.lse2[roff];  // +inf on padded rows: P = 0 there
     const float Drow = p.delta[roff];
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
@@ -235,28 +243,30 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t s_addr = tmem + COL_S + 64u * (j & 1) + lane_off;
       const uint32_t dp_addr = tmem + COL_DP + 64u * (j & 1) + lane_off;
-      const int kvb = j * BKV;
-      uint32_t w[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(s_addr + c * 32, us);
-        tmem_ld32(dp_addr + c * 32, ud);
-        tmem_wait_ld();
+      const int kv_first = j * BKV + 32 * half;  // this thread's first key column
+      uint32_t us[32], ud[32], w[16];
+      tmem_ld32(s_addr + 32 * half, us);
+      tmem_ld32(dp_addr + 32 * half, ud);
+      tmem_wait_ld();
+      if (kv_first + 31 <= limit) {  // every key of the half-tile visible
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          float d2[2];
+          const float p0 = ex2_approx(fmaf(__uint_as_float(us[2 * k]), p.scale_log2, -lse2));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(us[2 * k + 1]), p.scale_log2, -lse2));
+          w[k] = pack_bf16x2(p0 * (__uint_as_float(ud[2 * k]) - Drow), p1 * (__uint_as_float(ud[2 * k + 1]) - Drow));
+        }
+      } else {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int kk = 2 * k + e;
-            const bool vis = kvb + c * 32 + kk <= limit;
-            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(us[kk]), p.scale_log2, -lse2)) : 0.f;
-            d2[e] = pv * (__uint_as_float(ud[kk]) - Drow);
-          }
-          w[c * 16 + k] = pack_bf16x2(d2[0], d2[1]);
+        for (int k = 0; k < 16; ++k) {
+          const bool v0 = kv_first + 2 * k <= limit, v1 = kv_first + 2 * k + 1 <= limit;
+          const float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(us[2 * k]), p.scale_log2, -lse2)) : 0.f;
+          const float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(us[2 * k + 1]), p.scale_log2, -lse2)) : 0.f;
+          w[k] = pack_bf16x2(p0 * (__uint_as_float(ud[2 * k]) - Drow), p1 * (__uint_as_float(ud[2 * k + 1]) - Drow));
         }
       }
-      tmem_st32(s_addr, w);
+      // dS packed in place over this half's own score columns (key pair k -> column 32*half + k),
+      // so the other warpgroup's scores are never overwritten before it has read them
+      tmem_st16(s_addr + 32 * half, w);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -267,7 +277,7 @@ __global__ void __launch_bounds__(192, 1)
       const bool valid = q_row < p.Sq;
       bf16* dst = p.dq + ((static_cast<long long>(b) * p.Sq + q_row) * p.n_h + h) * 192;
 #pragma unroll 1
-      for (int c = 0; c < 6; ++c) {
+      for (int c = 3 * half; c < 3 * half + 3; ++c) {
         uint32_t u[32];
         tmem_ld32(tmem + COL_DQ + lane_off + c * 32, u);  // warp-collective: every lane takes part
         tmem_wait_ld();
@@ -359,7 +369,7 @@ LaunchResult tc_attn_bwd_dq(const Dims& d, const bf16* q, const bf16* k_rope, co
     r.what = "cudaFuncSetAttribute(attn_bwd_dq)";
     return r;
   }
-  attn_bwd_dq_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), 192, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
+  attn_bwd_dq_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_bwd_dq_kernel launch";
   return r;

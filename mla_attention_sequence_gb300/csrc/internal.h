@@ -50,7 +50,8 @@ LaunchResult simt_fwd(const Dims& d, bool is_bf16, const void* q, const void* c_
                       const void* W_UK, const void* W_UV, void* out, float* lse, void* ws, cudaStream_t st);
 LaunchResult simt_bwd(const Dims& d, bool is_bf16, const void* q, const void* c_kv, const void* k_rope,
                       const void* W_UK, const void* W_UV, const void* out, const float* lse, const void* dout,
-                      void* dq, void* dc_kv, void* dk_rope, void* dW_UK, void* dW_UV, void* ws, cudaStream_t st);
+                      void* dq, void* dc_kv, void* dk_rope, void* dW_UK, void* dW_UV, void* ws, bool reuse_kv,
+                      cudaStream_t st);
 
 // ---- tensor-core path (bf16, d_c=512, d_nope=d_v=128, d_rope=64).
 bool tc_supported(const Dims& d);

@@ -324,10 +324,10 @@ LaunchResult fwd_t(const Dims& d, const T* q, const T* c_kv, const T* k_rope, co
 template <typename T>
 LaunchResult bwd_t(const Dims& d, const T* q, const T* c_kv, const T* k_rope, const T* W_UK, const T* W_UV,
                    const T* out, const float* lse, const T* dout, T* dq, T* dc_kv, T* dk_rope, T* dW_UK, T* dW_UV,
-                   void* ws, cudaStream_t st) {
+                   void* ws, bool reuse_kv, cudaStream_t st) {
   LaunchResult r;
   SimtWs w = carve(d, ws, true);
-  r.err = recon(d, c_kv, W_UK, W_UV, w.kn, w.v, st);
+  if (!reuse_kv) r.err = recon(d, c_kv, W_UK, W_UV, w.kn, w.v, st);
   if (r.err != cudaSuccess) {
     r.what = "simt reconstruct";
     return r;
@@ -413,16 +413,19 @@ LaunchResult simt_fwd(const Dims& d, bool is_bf16, const void* q, const void* c_
 
 LaunchResult simt_bwd(const Dims& d, bool is_bf16, const void* q, const void* c_kv, const void* k_rope,
                       const void* W_UK, const void* W_UV, const void* out, const float* lse, const void* dout,
-                      void* dq, void* dc_kv, void* dk_rope, void* dW_UK, void* dW_UV, void* ws, cudaStream_t st) {
+                      void* dq, void* dc_kv, void* dk_rope, void* dW_UK, void* dW_UV, void* ws, bool reuse_kv,
+                      cudaStream_t st) {
   if (is_bf16)
     return bwd_t(d, static_cast<const bf16*>(q), static_cast<const bf16*>(c_kv), static_cast<const bf16*>(k_rope),
                  static_cast<const bf16*>(W_UK), static_cast<const bf16*>(W_UV), static_cast<const bf16*>(out), lse,
                  static_cast<const bf16*>(dout), static_cast<bf16*>(dq), static_cast<bf16*>(dc_kv),
-                 static_cast<bf16*>(dk_rope), static_cast<bf16*>(dW_UK), static_cast<bf16*>(dW_UV), ws, st);
+                 static_cast<bf16*>(dk_rope), static_cast<bf16*>(dW_UK), static_cast<bf16*>(dW_UV), ws, reuse_kv,
+                 st);
   return bwd_t(d, static_cast<const float*>(q), static_cast<const float*>(c_kv), static_cast<const float*>(k_rope),
                static_cast<const float*>(W_UK), static_cast<const float*>(W_UV), static_cast<const float*>(out), lse,
                static_cast<const float*>(dout), static_cast<float*>(dq), static_cast<float*>(dc_kv),
-               static_cast<float*>(dk_rope), static_cast<float*>(dW_UK), static_cast<float*>(dW_UV), ws, st);
+               static_cast<float*>(dk_rope), static_cast<float*>(dW_UK), static_cast<float*>(dW_UV), ws, reuse_kv,
+               st);
 }
 
 }  // namespace laga

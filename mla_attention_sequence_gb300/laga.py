@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "LAGA_OK", 1: "LAGA_ERR_INVALID_ARG", 2: "LAGA_ERR_UNSUPPORTE
                 4: "LAGA_ERR_CUDA", 5: "LAGA_ERR_TIMEOUT"}
 DTYPES = {"f32": 0, "bf16": 1}
 VARIANTS = {"auto": 0, "materialize": 1, "fused_recon": 2, "simt": 3}
+FLAG_REUSE_KV = 1
 
 EXPORTS = ("laga_mla_fwd_workspace_size", "laga_mla_bwd_workspace_size", "laga_mla_fwd", "laga_mla_bwd",
            "laga_mla_reconstruct", "laga_mla_check", "laga_status_string", "laga_mla_last_error",
@@ -34,7 +35,7 @@ class LagaDesc(ctypes.Structure):
                 ("n_h", ctypes.c_int64), ("d_c", ctypes.c_int64), ("d_nope", ctypes.c_int64),
                 ("d_rope", ctypes.c_int64), ("d_v", ctypes.c_int64), ("q_offset", ctypes.c_int64),
                 ("causal", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("variant", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class LagaError(RuntimeError):
@@ -83,9 +84,9 @@ def _raise_if(status: int):
         raise LagaError(status, lib().laga_mla_last_error().decode(errors="replace"))
 
 
-def make_desc(p: Problem, softmax_scale: float | None = None, variant: str = "auto") -> LagaDesc:
+def make_desc(p: Problem, softmax_scale: float | None = None, variant: str = "auto", flags: int = 0) -> LagaDesc:
     return LagaDesc(p.B, p.Sq, p.S, p.n_h, p.d_c, p.d_nope, p.d_rope, p.d_v, p.q_offset, 1 if p.causal else 0,
-                    float(softmax_scale) if softmax_scale else 0.0, DTYPES[p.dtype], VARIANTS[variant])
+                    float(softmax_scale) if softmax_scale else 0.0, DTYPES[p.dtype], VARIANTS[variant], flags)
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -164,13 +165,19 @@ def fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset: int = 0, causal: bool = True, sof
 
 def bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, q_offset: int = 0, causal: bool = True,
         softmax_scale: float | None = None, variant: str = "auto", workspace: torch.Tensor | None = None,
-        grads: dict | None = None):
-    """laga_mla_bwd: returns dict dq, dc_kv, dk_rope, dW_UK, dW_UV."""
+        grads: dict | None = None, reuse_kv: bool = False):
+    """laga_mla_bwd: returns dict dq, dc_kv, dk_rope, dW_UK, dW_UV.
+
+    reuse_kv=True (LAGA_FLAG_REUSE_KV): `workspace` is the buffer the forward
+    ran with, still holding the K_nope/V it rebuilt; the backward reads them
+    instead of rebuilding them."""
     p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal)
     for t in (out, lse, dout):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("out, lse and dout must be contiguous CUDA tensors")
-    d = make_desc(p, softmax_scale, variant)
+    if reuse_kv and workspace is None:
+        raise ValueError("reuse_kv needs the workspace the forward ran with")
+    d = make_desc(p, softmax_scale, variant, FLAG_REUSE_KV if reuse_kv else 0)
     L = lib()
     dev = q.device
     g = grads if grads is not None else {
@@ -207,14 +214,15 @@ def check(device=None) -> None:
 
 @dataclass
 class StepBuffers:
-    """Preallocated device buffers for repeated forward+backward steps of one problem."""
+    """Preallocated device buffers for repeated forward+backward steps of one
+    problem. One workspace serves both calls: the backward reuses the K_nope/V
+    the forward left in it."""
     p: Problem
     inputs: dict
     out: torch.Tensor
     lse: torch.Tensor
     grads: dict
-    ws_fwd: torch.Tensor | None
-    ws_bwd: torch.Tensor | None
+    ws: torch.Tensor | None
 
 
 def alloc_step(p: Problem, inputs: dict, variant: str = "auto") -> StepBuffers:
@@ -225,17 +233,16 @@ def alloc_step(p: Problem, inputs: dict, variant: str = "auto") -> StepBuffers:
     grads = {"dq": torch.empty_like(inputs["q"]), "dc_kv": torch.empty_like(inputs["c_kv"]),
              "dk_rope": torch.empty_like(inputs["k_rope"]), "dW_UK": torch.empty_like(inputs["W_UK"]),
              "dW_UV": torch.empty_like(inputs["W_UV"])}
-    nf, nb = fwd_workspace_bytes(p, variant), bwd_workspace_bytes(p, variant)
-    wf = torch.empty(nf, dtype=torch.uint8, device=dev) if nf else None
-    wb = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
-    return StepBuffers(p, inputs, out, lse, grads, wf, wb)
+    nb = max(fwd_workspace_bytes(p, variant), bwd_workspace_bytes(p, variant))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+    return StepBuffers(p, inputs, out, lse, grads, ws)
 
 
 def step(buf: StepBuffers, variant: str = "auto"):
     """One forward + backward pass of the attention block into preallocated buffers."""
     x, p = buf.inputs, buf.p
     fwd(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], p.q_offset, p.causal, None, variant,
-        buf.ws_fwd, buf.out, buf.lse)
+        buf.ws, buf.out, buf.lse)
     bwd(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], buf.out, buf.lse, x["dout"], p.q_offset, p.causal,
-        None, variant, buf.ws_bwd, buf.grads)
+        None, variant, buf.ws, buf.grads, reuse_kv=buf.ws is not None)
     return buf.out, buf.lse, buf.grads

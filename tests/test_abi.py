@@ -74,6 +74,13 @@ def test_invalid_arguments_are_rejected_before_launch(L):
     assert call_fwd(L, desc(Sq=0)) == 1
 
 
+def test_unknown_flag_bits_rejected(L):
+    d = desc()
+    d.flags = 2
+    assert call_fwd(L, d) == 1
+    assert b"flags" in L.laga_mla_last_error()
+
+
 def test_unsupported_tensor_core_dims(L):
     d = desc(d_c=256, variant="materialize")
     assert call_fwd(L, d) == 2

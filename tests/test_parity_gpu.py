@@ -228,6 +228,26 @@ def test_sequence_parallel_shards_on_gpu():
         assert np.abs(sums[k] - ref).max() <= 2e-2 * np.abs(ref).max(), k
 
 
+@pytest.mark.parametrize("variant", ["auto", "simt"])
+def test_backward_reusing_forward_kv_matches(variant):
+    """LAGA_FLAG_REUSE_KV: a backward that reads the forward's K_nope/V from the
+    shared workspace gives bitwise the same gradients as one that rebuilds them."""
+    p = small(B=2, n_h=3, Sq=200, S=520, q_offset=300)
+    x = make_inputs(p, seed=15)
+    t = to_dev(x, p)
+    nb = max(laga.fwd_workspace_bytes(p, variant), laga.bwd_workspace_bytes(p, variant))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev())
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True, None, variant, ws)
+    g1 = laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True,
+                  None, variant, ws, reuse_kv=True)
+    g1 = {k: v.clone() for k, v in g1.items()}
+    g2 = laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True,
+                  None, variant)
+    laga.check(dev())
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+
+
 def test_determinism():
     p = small(B=1, n_h=4, Sq=512, S=1024, q_offset=512)
     x = make_inputs(p, seed=14)
