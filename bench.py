@@ -359,6 +359,72 @@ def run_ours(args, p: Problem):
     return 0
 
 
+# ---------------------------------------------------------------- forward variants
+def run_variant_sweep(args):
+    """Forward of the two K/V variants over the last-rank SP=8 sweep shapes:
+    'materialize' (reconstruction GEMM to HBM + attention) against
+    'fused_recon' (K/V tiles rebuilt inside the attention kernel). Same
+    algorithmic flops for both (attention + one reconstruction of the visible
+    latent prefix); one JSON line per shape and variant."""
+    import torch
+
+    from mla_attention_sequence_gb300 import build as build_mod
+    from mla_attention_sequence_gb300 import laga
+    from mla_attention_sequence_gb300.configs import sweep_points
+
+    build_mod.build()
+    L = laga.lib()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for p in sweep_points():
+        if args.sweep_filter and args.sweep_filter not in p.name:
+            continue
+        x = make_inputs(p, SEED, with_dout=False)
+        t = {k: torch.from_numpy(v).to(dev).to(torch.bfloat16) for k, v in x.items()}
+        out = torch.empty((p.B, p.Sq, p.n_h, p.d_v), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((p.B, p.n_h, p.Sq), dtype=torch.float32, device=dev)
+        for variant in ("materialize", "fused_recon"):
+            nbytes = laga.fwd_workspace_bytes(p, variant)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+
+            def run():
+                laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal, None, variant,
+                         ws, out, lse)
+            for _ in range(args.warmup):
+                run()
+            laga.check(dev)
+            L.laga_mla_profile_enable(1)
+            times = []
+            for _ in range(args.steps):
+                flush.zero_()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                run()
+                e.record(stream)
+                torch.cuda.synchronize()
+                times.append(s.elapsed_time(e))
+            import ctypes
+            nmax = 16 * args.steps
+            names = (ctypes.c_char_p * nmax)()
+            ms = (ctypes.c_float * nmax)()
+            n = L.laga_mla_profile_read(ctypes.cast(names, ctypes.POINTER(ctypes.c_char_p)), ms, nmax)
+            L.laga_mla_profile_enable(0)
+            per = {}
+            for i in range(min(n, nmax)):
+                per.setdefault(names[i].decode(), []).append(ms[i])
+            t_ms = float(np.median(times))
+            print(json.dumps({"mode": "variant_sweep", "workload": p.name, "S": p.S, "n_h": p.n_h, "Sq": p.Sq,
+                              "variant": variant, "ms_fwd": t_ms,
+                              "tflops_fwd": p.flops_fwd() / (t_ms * 1e-3) / 1e12,
+                              "kernels_ms": {k: float(np.median(v)) for k, v in per.items()},
+                              "workspace_bytes": nbytes}), flush=True)
+            del ws
+        del t
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -369,9 +435,14 @@ def main(argv=None):
     ap.add_argument("--variant", default="auto", choices=["auto", "materialize", "simt"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant-sweep", action="store_true",
+                    help="time the forward of both K/V variants over the sweep shapes instead")
+    ap.add_argument("--sweep-filter", default="", help="only sweep shapes whose name contains this string")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
     p = NAMED[args.workload]
+    if args.variant_sweep:
+        return run_variant_sweep(args)
     if args.impl == "reference":
         return run_reference(args, p)
     return run_ours(args, p)

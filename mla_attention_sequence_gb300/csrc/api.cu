@@ -140,8 +140,11 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
     return Path::Invalid;
   }
   if (x.variant == LAGA_VARIANT_FUSED_RECON) {
-    *st = fail(LAGA_ERR_UNSUPPORTED, "LAGA_VARIANT_FUSED_RECON is not available in this build%s");
-    return Path::Invalid;
+    if (for_bwd) {
+      *st = fail(LAGA_ERR_UNSUPPORTED, "LAGA_VARIANT_FUSED_RECON is forward-only%s");
+      return Path::Invalid;
+    }
+    return Path::TensorCoreFused;
   }
   if (tc_ok && !want_simt) return Path::TensorCore;
   // CUDA-core path limits (shared-memory rows of scores).
@@ -240,9 +243,11 @@ laga_status laga_mla_fwd(const laga_mla_desc* desc, const void* q, const void* c
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = desc->dtype == LAGA_DTYPE_BF16;
   if (path == Path::TensorCoreFused) {
-    return from_launch(tc_attn_fwd_fused(d, static_cast<const bf16*>(q), static_cast<const bf16*>(c_kv),
-                                         static_cast<const bf16*>(W_UK), static_cast<const bf16*>(W_UV),
-                                         static_cast<const bf16*>(k_rope), static_cast<bf16*>(out), lse, s));
+    return from_launch(timed("attn_fwd_fused", s, [&] {
+      return tc_attn_fwd_fused(d, static_cast<const bf16*>(q), static_cast<const bf16*>(c_kv),
+                               static_cast<const bf16*>(W_UK), static_cast<const bf16*>(W_UV),
+                               static_cast<const bf16*>(k_rope), static_cast<bf16*>(out), lse, s);
+    }));
   }
   const size_t need = path == Path::Simt ? simt_fwd_workspace(d) : tc_fwd_workspace(d);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))

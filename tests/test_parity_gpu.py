@@ -130,12 +130,13 @@ TC_CASES = {
 }
 
 
+@pytest.mark.parametrize("variant", ["materialize", "fused_recon"])
 @pytest.mark.parametrize("name", list(TC_CASES))
-def test_tensor_core_forward(name):
+def test_tensor_core_forward(name, variant):
     p = TC_CASES[name]
     x = make_inputs(p, seed=10)
-    assert_close(run_gpu(p, x, "materialize", backward=False), run_oracle(p, x, backward=False), TOL["bf16"],
-                 tag=name)
+    assert_close(run_gpu(p, x, variant, backward=False), run_oracle(p, x, backward=False), TOL["bf16"],
+                 tag=f"{name} {variant}")
 
 
 @pytest.mark.parametrize("name", list(TC_CASES))
@@ -246,6 +247,18 @@ def test_backward_reusing_forward_kv_matches(variant):
     laga.check(dev())
     for k in g1:
         assert torch.equal(g1[k], g2[k]), k
+
+
+def test_fused_reconstruction_matches_materialized_at_full_size():
+    """Both forward variants on the DSV3 last-rank shard: same outputs within the
+    bf16 tolerance (they round K/V to bf16 at the same point)."""
+    p = DSV3_LAST_RANK
+    x = make_inputs(p, seed=2008, with_dout=False)
+    t = to_dev(x, p)
+    oa, la = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True, None, "materialize")
+    ob, lb = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True, None, "fused_recon")
+    laga.check(dev())
+    assert_close({"out": ob, "lse": lb}, {"out": np64(oa), "lse": np64(la)}, TOL["bf16"], tag="fused vs materialized")
 
 
 def test_determinism():
