@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-from mla_attention_sequence_gb300.configs import NAMED, DSV3_LAST_RANK, Problem  # noqa: E402
+from mla_attention_sequence_gb300.configs import GROUPS, NAMED, DSV3_LAST_RANK, Problem  # noqa: E402
 from mla_attention_sequence_gb300.synth import make_inputs  # noqa: E402
 
 METRIC = "MLA attn-block fwd+bwd TFLOP/s & tokens/s, % of GB300 bf16 peak"
@@ -215,7 +215,36 @@ def run_reference(args, p: Problem):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, p: Problem):
+def shard_inputs(name: str, seed: int):
+    """Problems of one step and their host inputs. A single shard draws its own
+    inputs; the all-ranks group draws the full sequence once and gives each rank
+    its query / dout rows with the shared latent, RoPE key and weights."""
+    if name not in GROUPS:
+        p = NAMED[name]
+        return [p], [make_inputs(p, seed)]
+    shards = GROUPS[name]
+    p0 = shards[0]
+    full = p0.with_(Sq=p0.S, q_offset=0)
+    x = make_inputs(full, seed)
+    xs = []
+    for p in shards:
+        rows = slice(p.q_offset, p.q_offset + p.Sq)
+        xs.append({k: (np.ascontiguousarray(v[:, rows]) if k in ("q", "dout") else v) for k, v in x.items()})
+    return shards, xs
+
+
+def kernel_flops(p: Problem) -> dict:
+    """Algorithmic flops each timed step of one shard's forward+backward owns."""
+    attn_fwd = 2 * p.pairs * p.n_h * (p.d_qk + p.d_v)
+    recon = 2 * p.B * p.skv_eff * p.d_c * p.n_h * (p.d_nope + p.d_v)
+    # backward attention = 2 x forward, split by the products each kernel owns:
+    # dK/dV kernel dV + dP + dK (128 + 128 + 192 per pair and head), dq kernel dQ (192)
+    unit = 2 * p.pairs * p.n_h
+    return {"attn_fwd": attn_fwd, "attn_bwd_dkdv": unit * (p.d_v + p.d_v + p.d_qk), "attn_bwd_dq": unit * p.d_qk,
+            "recon_fwd_gemm": recon, "recon_bwd_dc_gemm": recon, "recon_bwd_dw_gemm": recon}
+
+
+def run_ours(args, name: str):
     import ctypes
 
     import torch
@@ -230,25 +259,37 @@ def run_ours(args, p: Problem):
     build_mod.build()
     L = laga.lib()
 
-    x = make_inputs(p, SEED + rank)
-    dt = torch.bfloat16 if p.dtype == "bf16" else torch.float32
-    host = {k: torch.from_numpy(v).to(dt).pin_memory() for k, v in x.items()}
-    dinp = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+    problems, xs = shard_inputs(name, SEED + rank)
+    dt = torch.bfloat16 if problems[0].dtype == "bf16" else torch.float32
+    shared = {}
+    dinps = []
+    for x in xs:
+        d = {}
+        for k, v in x.items():
+            key = (k, id(v))
+            if key not in shared:  # inputs shared by shards are staged once
+                hv = torch.from_numpy(v).to(dt).pin_memory()
+                shared[key] = (hv, hv.to(dev, non_blocking=True))
+            d[k] = shared[key][1]
+        dinps.append(d)
     torch.cuda.synchronize()
-    buf = laga.alloc_step(p, dinp, args.variant)
+    bufs = [laga.alloc_step(p, d, args.variant) for p, d in zip(problems, dinps)]
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def step():
+        for buf in bufs:
+            laga.step(buf, args.variant)
+
     for _ in range(args.warmup):
-        laga.step(buf, args.variant)
+        step()
     laga.check(dev)
     torch.cuda.synchronize()
 
     # ---- device-resident timed region
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    clocks = ClockSampler(local)
     L.laga_mla_profile_enable(1)
     barrier(world)
     torch.cuda.synchronize()
@@ -256,12 +297,12 @@ def run_ours(args, p: Problem):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        laga.step(buf, args.variant)
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    nmax = 64 * args.steps
+    nmax = 64 * args.steps * len(bufs)
     names = (ctypes.c_char_p * nmax)()
     ms = (ctypes.c_float * nmax)()
     nrec = L.laga_mla_profile_read(ctypes.cast(names, ctypes.POINTER(ctypes.c_char_p)), ms, nmax)
@@ -271,16 +312,18 @@ def run_ours(args, p: Problem):
     total_ms = reduce_max(sum(step_ms), world, dev)
     per_kernel = {}
     for i in range(min(nrec, nmax)):
-        n = names[i].decode()
-        per_kernel.setdefault(n, []).append(ms[i])
+        per_kernel.setdefault(names[i].decode(), []).append(ms[i])
 
     # ---- end-to-end through the public API with host buffers
-    out_host = {"out": torch.empty(buf.out.shape, dtype=dt).pin_memory(),
-                "lse": torch.empty(buf.lse.shape, dtype=torch.float32).pin_memory()}
-    for k, v in buf.grads.items():
-        out_host[k] = torch.empty(v.shape, dtype=dt).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+    outs_host = []
+    for buf in bufs:
+        oh = {"out": torch.empty(buf.out.shape, dtype=dt).pin_memory(),
+              "lse": torch.empty(buf.lse.shape, dtype=torch.float32).pin_memory()}
+        for k, v in buf.grads.items():
+            oh[k] = torch.empty(v.shape, dtype=dt).pin_memory()
+        outs_host.append(oh)
+    h2d = sum(hv.numel() * hv.element_size() for hv, _ in shared.values())
+    d2h = sum(v.numel() * v.element_size() for oh in outs_host for v in oh.values())
     e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
@@ -288,59 +331,64 @@ def run_ours(args, p: Problem):
     for i in range(args.steps):
         flush.zero_()
         e_start[i].record(stream)
-        for k in dinp:
-            dinp[k].copy_(host[k], non_blocking=True)
-        laga.step(buf, args.variant)
-        out_host["out"].copy_(buf.out, non_blocking=True)
-        out_host["lse"].copy_(buf.lse, non_blocking=True)
-        for k, v in buf.grads.items():
-            out_host[k].copy_(v, non_blocking=True)
+        for hv, dv in shared.values():
+            dv.copy_(hv, non_blocking=True)
+        for buf, oh in zip(bufs, outs_host):
+            laga.step(buf, args.variant)
+            oh["out"].copy_(buf.out, non_blocking=True)
+            oh["lse"].copy_(buf.lse, non_blocking=True)
+            for k, v in buf.grads.items():
+                oh[k].copy_(v, non_blocking=True)
         e_end[i].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)), world, dev)
 
-    flops = p.flops_step()
+    flops = sum(p.flops_step() for p in problems)
+    tokens = sum(p.B * p.Sq for p in problems)
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
     e2e_value = world * flops * args.steps / (e2e_ms * 1e-3) / 1e12
-    tokens_s = world * p.B * p.Sq * args.steps / (total_ms * 1e-3)
+    tokens_s = world * tokens * args.steps / (total_ms * 1e-3)
     peaks = load_peaks()
 
-    # roofline of the dominant kernel (largest total time)
+    # roofline of the dominant kernel (largest total time): algorithmic flops of
+    # all its launches in a step over their measured time in that step
+    kflops = {}
+    for p in problems:
+        for k, v in kernel_flops(p).items():
+            kflops[k] = kflops.get(k, 0) + v
     kernel_ms = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     dom = max(per_kernel, key=lambda k: sum(per_kernel[k])) if per_kernel else None
-    attn_fwd_flops = 2 * p.pairs * p.n_h * (p.d_qk + p.d_v)
-    recon_flops = 2 * p.B * p.skv_eff * p.d_c * p.n_h * (p.d_nope + p.d_v)
-    # backward attention = 2 x forward, split by the products each kernel owns:
-    # dK/dV kernel dV + dP + dK (128 + 128 + 192 per pair and head), dq kernel dQ (192)
-    unit = 2 * p.pairs * p.n_h
-    alg = {"attn_fwd": attn_fwd_flops, "attn_bwd_dkdv": unit * (p.d_v + p.d_v + p.d_qk),
-           "attn_bwd_dq": unit * p.d_qk, "recon_fwd_gemm": recon_flops,
-           "recon_bwd_dc_gemm": recon_flops, "recon_bwd_dw_gemm": recon_flops}
     roof = None
-    if dom in alg:
-        achieved = alg[dom] / (kernel_ms[dom] * 1e-3) / 1e12
+    if dom in kflops:
+        t_step = sum(per_kernel[dom]) / args.steps
+        achieved = kflops[dom] / (t_step * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None,
                 "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
-                "flops_per_launch": alg[dom], "ms_per_launch": kernel_ms[dom]}
+                "flops_per_launch": kflops[dom] / len(problems), "ms_per_launch": t_step / len(problems),
+                "launches_per_step": len(problems)}
     launches_per_step = {"simt_fwd": 3, "simt_bwd": 10}  # every other timed step is one kernel
     gpu_launches = sum(launches_per_step.get(k, 1) * len(v) for k, v in per_kernel.items())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, heads, secs = time_oracle(p, x, budget_s=args.cpu_budget)
+        tf, heads, secs = time_oracle(problems[-1], xs[-1], budget_s=args.cpu_budget)
         cpu = {"value": tf, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": f"fp64 oracle fwd+bwd of {heads} head(s) (of {p.n_h}) of the same shard, {secs:.1f} s; "
-                         f"TFLOP/s of the sample's algorithmic flops"}
+               "sample": f"fp64 oracle fwd+bwd of {heads} head(s) (of {problems[-1].n_h}) of shard "
+                         f"{problems[-1].name}, {secs:.1f} s; TFLOP/s of the sample's algorithmic flops"}
 
     if rank == 0:
+        cfg = workload_config(problems[-1], {"variant": args.variant})
+        if len(problems) > 1:
+            cfg.update({"workload": name, "Sq": tokens, "q_offset": [p.q_offset for p in problems],
+                        "shards_per_step": len(problems), "flops_per_step": flops, "tokens_per_step": tokens})
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(p, {"variant": args.variant}),
+            "config": cfg,
             "tokens_per_s": tokens_s,
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "peak_source": peaks["source"],
@@ -431,7 +479,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DSV3_LAST_RANK.name, choices=sorted(NAMED))
+    ap.add_argument("--workload", default=DSV3_LAST_RANK.name, choices=sorted(NAMED) + sorted(GROUPS))
     ap.add_argument("--variant", default="auto", choices=["auto", "materialize", "simt"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -440,12 +488,12 @@ def main(argv=None):
     ap.add_argument("--sweep-filter", default="", help="only sweep shapes whose name contains this string")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
-    p = NAMED[args.workload]
     if args.variant_sweep:
         return run_variant_sweep(args)
     if args.impl == "reference":
+        p = GROUPS[args.workload][-1] if args.workload in GROUPS else NAMED[args.workload]
         return run_reference(args, p)
-    return run_ours(args, p)
+    return run_ours(args, args.workload)
 
 
 if __name__ == "__main__":

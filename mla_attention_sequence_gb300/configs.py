@@ -93,3 +93,8 @@ def sweep_points():
 
 NAMED = {p.name: p for p in [TINY_F32, MID_BF16] + [dsv3_rank(r) for r in range(8)]
          + list(sweep_points())}
+
+# Workloads made of several shards run back to back in one step: every SP=8
+# rank of the DeepSeek-V3 layer in turn (q_offset = 2048 r), i.e. the whole
+# 16384-token sequence's attention block as eight rank-local calls.
+GROUPS = {"dsv3_sp8_all_ranks_S16384_h128": [dsv3_rank(r) for r in range(8)]}

@@ -203,6 +203,66 @@ def test_dsv3_last_rank_sampled_heads_and_identities():
     assert abs(a_c - (a_uk + a_uv)) <= 2e-2 * scale_
 
 
+@pytest.mark.parametrize("r", range(8))
+def test_dsv3_every_rank_shard_sampled(r):
+    """Every SP=8 rank shard of the DeepSeek-V3 layer (q_offset = 2048 r), forward and
+    backward at full size: one head per rank against the per-head oracle, plus
+    the gradient identities over all heads."""
+    from mla_attention_sequence_gb300.configs import dsv3_rank
+    p = dsv3_rank(r)
+    x = make_inputs(p, seed=3000 + r)
+    t = to_dev(x, p)
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True)
+    g = laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True)
+    laga.check(dev())
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    h = (37 * r + 5) % p.n_h
+    ref = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
+                                   0, h, p.q_offset, True)
+    got = {"out": out[0, :, h], "lse": lse[0, h], "dq": g["dq"][0, :, h],
+           "dW_UK": g["dW_UK"][:, h * 128:(h + 1) * 128], "dW_UV": g["dW_UV"][:, h * 128:(h + 1) * 128]}
+    want = {"out": ref["out_h"], "lse": ref["lse_h"], "dq": ref["dq_h"], "dW_UK": ref["dW_UK_h"],
+            "dW_UV": ref["dW_UV_h"]}
+    assert_close(got, want, TOL["bf16"], tag=f"rank {r} head {h}")
+    # latent rows beyond the shard's causal prefix get no gradient
+    tail = p.q_offset + p.Sq
+    assert not g["dc_kv"][:, tail:].any() and not g["dk_rope"][:, tail:].any()
+
+    def inner(a, b):
+        return float((np64(a) * b).sum())
+    a_q = inner(g["dq"], x64["q"])
+    a_o = inner(out, x64["dout"])
+    scale_ = max(abs(a_q), abs(a_o), 1.0)
+    assert abs(inner(g["dW_UV"], x64["W_UV"]) - a_o) <= 2e-2 * scale_
+    assert abs(inner(g["dW_UK"], x64["W_UK"]) + inner(g["dk_rope"], x64["k_rope"]) - a_q) <= 2e-2 * scale_
+
+
+@pytest.mark.parametrize("seq,n_h", [(4096, 32), (32768, 32), (8192, 128)])
+def test_sweep_shapes_sampled(seq, n_h):
+    """Last-rank SP=8 shards of the sweep (sequence length x heads), both forward
+    variants and the backward, one head against the per-head oracle."""
+    from mla_attention_sequence_gb300.configs import dsv3_rank
+    p = dsv3_rank(7, seq=seq, n_h=n_h)
+    x = make_inputs(p, seed=seq + n_h)
+    t = to_dev(x, p)
+    outs = {v: laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True, None, v)
+            for v in ("materialize", "fused_recon")}
+    out, lse = outs["materialize"]
+    g = laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True)
+    laga.check(dev())
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    h = n_h - 1
+    ref = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
+                                   0, h, p.q_offset, True)
+    for v, (o, l) in outs.items():
+        assert_close({"out": o[0, :, h], "lse": l[0, h]}, {"out": ref["out_h"], "lse": ref["lse_h"]}, TOL["bf16"],
+                     tag=f"sweep S={seq} n_h={n_h} {v}")
+    assert_close({"dq": g["dq"][0, :, h], "dW_UK": g["dW_UK"][:, h * 128:(h + 1) * 128],
+                  "dW_UV": g["dW_UV"][:, h * 128:(h + 1) * 128]},
+                 {"dq": ref["dq_h"], "dW_UK": ref["dW_UK_h"], "dW_UV": ref["dW_UV_h"]}, TOL["bf16"],
+                 tag=f"sweep S={seq} n_h={n_h} backward")
+
+
 # ------------------------------------------------------------------ SP shards, determinism
 def test_sequence_parallel_shards_on_gpu():
     S, sp = 1024, 4
