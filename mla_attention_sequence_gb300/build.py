@@ -17,7 +17,10 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
-BUILD = os.path.join(HERE, "_build")
+# LAGA_BUILD_TRACE=1 builds a separate debug library with in-kernel event
+# tracing compiled in (see LAGA_TRACE in csrc/ptx.cuh).
+TRACE = os.environ.get("LAGA_BUILD_TRACE", "") == "1"
+BUILD = os.path.join(HERE, "_build_trace" if TRACE else "_build")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(BUILD, "liblaga_mla.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,6 +42,8 @@ def _flags(ptxas_verbose: bool):
          "--expt-relaxed-constexpr", "-Xcompiler", "-Wno-unused-function"]
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]
+    if TRACE:
+        f += ["-DLAGA_TRACE"]
     return f
 
 

@@ -17,7 +17,10 @@
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
 //   warps 2..9  two warpgroups; each thread owns one query row (TMEM lane) and
 //               half of the tile's 64 key columns: P, dS, and half the epilogue
-// TMEM columns: S/dS x2 [0,128), dP x2 [128,256), dq [256,448).
+// TMEM columns: S/dS x2 [0,128), dP x2 [128,256), dq [256,448), dO [448,512).
+// dO is the same for every key tile: the query-row warps copy it into TMEM
+// once and dP = dO V^T reads it from there (A operand from TMEM), which takes
+// its reads off the shared-memory port that bounds this kernel.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,7 +43,7 @@ constexpr int OFF_V = OFF_K + NSTAGE * K_BYTES;
 constexpr int OFF_BARS = OFF_V + NSTAGE * V_BYTES;
 constexpr int SMEM_BYTES = OFF_BARS + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DO = 448;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
 constexpr uint32_t IDESC_DQ = idesc_bf16(128, 192, false, true);
 constexpr int NTHREADS = 320;
@@ -81,7 +84,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* ds_full = bars + 15; // [2]  dS(j) in TMEM
   uint64_t* dq_done = bars + 17;
   uint64_t* drain = bars + 18;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* do_tmem = bars + 19;  // dO copied into TMEM by the query-row warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
+    mbar_init(do_tmem, SOFTMAX_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -164,11 +169,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait_or_abort(q_full, 0, abort_flag, 73);
+      bool ok = mbar_wait_or_abort(q_full, 0, abort_flag, 73) && mbar_wait_or_abort(do_tmem, 0, abort_flag, 77);
       bool issued = false;
       tc_fence_after();
       const uint32_t q_base = smem_u32(smem + OFF_Q);
-      const uint32_t do_base = smem_u32(smem + OFF_DO);
       auto issue_s_dp = [&](int j) -> bool {  // S(j) = Q K_j^T ; dP(j) = dO V_j^T
         const int s = j % NSTAGE;
         const uint32_t ph = (j / NSTAGE) & 1;
@@ -187,10 +191,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t v_base = smem_u32(smem + OFF_V + s * V_BYTES);
         const uint32_t dd = tmem + COL_DP + 64u * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < 8; ++kk) {  // head dims [16kk, 16kk + 16): dO columns [8kk, 8kk + 8)
           const uint32_t c = kk >> 2, k = kk & 3;
-          mma_ss(dd, sdesc_sw128(do_base + c * QBOX + k * 32, 16, 1024),
-                 sdesc_sw128(v_base + c * KBOX + k * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ts(dd, tmem + COL_DO + kk * 8, sdesc_sw128(v_base + c * KBOX + k * 32, 16, 1024), IDESC_S,
+                 kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[j & 1]);
         mma_commit(&v_empty[s]);
@@ -236,9 +240,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
       bool w = true;
       if (lane == 0) w = mbar_wait_or_abort(bar, parity, abort_flag, where);
-      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      const bool all = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      __syncwarp();  // order lane 0's acquire before the other lanes' reads
+      return all;
     };
-    for (int j = 0; j < n_kv; ++j) {
+    // dO row r -> TMEM lane r as packed bf16 pairs; warpgroup `half` copies
+    // head dims [64*half, 64*half + 64) (box `half` of the swizzled TMA tile).
+    if (!warp_wait(q_full, 0, 83)) ok = false;
+    if (ok) {
+      uint32_t w[32];
+      const uint8_t* box = smem + OFF_DO + half * QBOX;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(r, k));
+        w[4 * k + 0] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
+      }
+      tmem_st32(tmem + COL_DO + lane_off + 32 * half, w);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(do_tmem);
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
       if (!warp_wait(&s_full[j & 1], (j >> 1) & 1, 81)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_addr = tmem + COL_S + 64u * (j & 1) + lane_off;

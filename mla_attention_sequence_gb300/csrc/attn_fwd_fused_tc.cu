@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     bool w = true;
     if (lane == 0) w = mbar_wait_or_abort(bar, parity, abort_flag, where);
-    return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    const bool all = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    __syncwarp();  // order lane 0's acquire before the other lanes' reads
+    return all;
   };
 
   if (warp == 0) {

@@ -12,11 +12,17 @@
 //   warps 2..5  softmax: one query row per thread (TMEM lane), online max and
 //               sum in the log2 domain, P written back over S as bf16 pairs,
 //               O rescaled in TMEM when the running max grows, final epilogue
-// TMEM columns: S/P buffer 0 [0,128), S/P buffer 1 [128,256), O [256,384).
+// TMEM columns: S/P buffer 0 [0,128), S/P buffer 1 [128,256), O [256,384),
+// Q [384,480). Q is the same for every key tile, so the softmax warps copy it
+// into TMEM once and S = Q K^T reads it from there (A operand from TMEM): the
+// shared-memory port then only carries K for S, V for PV and the TMA writes,
+// which is what bounds this kernel.
 // MMA order S(0), S(1), PV(0), S(2), PV(1), ... lets softmax of tile j+1
 // overlap the PV product of tile j.
 #include "internal.h"
 #include "ptx.cuh"
+
+LAGA_TRACE_DEFINE(fwd)
 
 namespace laga {
 namespace {
@@ -30,6 +36,7 @@ constexpr int V_BYTES = 2 * BOX;
 constexpr int SMEM_BYTES = Q_BYTES + 2 * K_BYTES + 2 * V_BYTES + 1024 + 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
+constexpr uint32_t COL_Q = 384;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, false, true);
 constexpr float LOG2E = 1.4426950408889634f;
@@ -71,7 +78,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* p_full = bars + 11;  // [2]
   uint64_t* pv_done = bars + 13;
   uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* q_tmem = bars + 15;  // Q copied into TMEM by the softmax warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -94,6 +102,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(pv_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_tmem, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -120,6 +129,7 @@ __global__ void __launch_bounds__(192, 1)
       for (; j < n_kv; ++j) {
         const int s = j & 1;
         if (!mbar_wait_or_abort(&k_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, 11)) break;
+        LAGA_TRACE_POINT(fwd, 20, j);
         uint8_t* dst = sK + s * K_BYTES;
         mbar_arrive_expect_tx(&k_full[s], K_BYTES);
         const int row = b * p.skv_pad + j * BKV;
@@ -137,6 +147,7 @@ __global__ void __launch_bounds__(192, 1)
       for (; j < n_kv; ++j) {
         const int s = j & 1;
         if (!mbar_wait_or_abort(&v_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, 12)) break;
+        LAGA_TRACE_POINT(fwd, 21, j);
         uint8_t* dst = sV + s * V_BYTES;
         mbar_arrive_expect_tx(&v_full[s], V_BYTES);
         const int row = b * p.skv_pad + j * BKV;
@@ -148,15 +159,16 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait_or_abort(q_full, 0, abort_flag, 13);
+      bool ok = mbar_wait_or_abort(q_tmem, 0, abort_flag, 13);
       bool issued = false;
       tc_fence_after();
-      const uint32_t q_base = smem_u32(sQ);
       auto issue_pv = [&](int jj) -> bool {
         const int s = jj & 1;
         const uint32_t ph = (jj >> 1) & 1;
         if (!mbar_wait_or_abort(&p_full[s], ph, abort_flag, 14)) return false;
+        LAGA_TRACE_POINT(fwd, 3, jj);
         if (!mbar_wait_or_abort(&v_full[s], ph, abort_flag, 15)) return false;
+        LAGA_TRACE_POINT(fwd, 4, jj);
         tc_fence_after();
         const uint32_t v_base = smem_u32(sV + s * V_BYTES);
         const uint32_t p_tmem = tmem + s * 128;
@@ -167,6 +179,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         mma_commit(pv_done);
         mma_commit(&v_empty[s]);
+        LAGA_TRACE_POINT(fwd, 5, jj);
         return true;
       };
       for (int j = 0; j < n_kv && ok; ++j) {
@@ -175,19 +188,20 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
+        LAGA_TRACE_POINT(fwd, 1, j);
         tc_fence_after();
         const uint32_t k_base = smem_u32(sK + s * K_BYTES);
         const uint32_t d_tmem = tmem + s * 128;
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
+        for (int kk = 0; kk < 12; ++kk) {  // head dims [16kk, 16kk + 16): Q columns [8kk, 8kk + 8)
           const uint32_t c = kk >> 2, k = kk & 3;
-          const uint64_t ad = sdesc_sw128(q_base + c * BOX + k * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(k_base + c * BOX + k * 32, 16, 1024);
-          mma_ss(d_tmem, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ts(d_tmem, tmem + COL_Q + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
         }
         issued = true;
         mma_commit(&s_full[s]);
         mma_commit(&k_empty[s]);
+        LAGA_TRACE_POINT(fwd, 2, j);
         if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
       if (ok) ok = issue_pv(n_kv - 1);
@@ -210,7 +224,9 @@ __global__ void __launch_bounds__(192, 1)
     auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
       bool w = true;
       if (lane == 0) w = mbar_wait_or_abort(bar, parity, abort_flag, where);
-      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      const bool all = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      __syncwarp();  // order lane 0's acquire before the other lanes' reads
+      return all;
     };
     auto wait_pv = [&](int upto) -> bool {  // until PV(upto) has completed
       while (pv_seen <= upto) {
@@ -219,6 +235,30 @@ __global__ void __launch_bounds__(192, 1)
       }
       return true;
     };
+    // Q row r -> TMEM lane r as packed bf16 pairs (the A-operand layout of a
+    // TS-MMA): 16-byte chunk k of box c sits at row r of the 128-byte-swizzled
+    // tile the TMA wrote, and becomes TMEM columns [32c + 4k, 32c + 4k + 4).
+    if (!warp_wait(q_full, 0, 20)) ok = false;
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < 3; ++c) {
+        uint32_t w[32];
+        const uint8_t* box = sQ + c * BOX;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(r, k));
+          w[4 * k + 0] = v.x;
+          w[4 * k + 1] = v.y;
+          w[4 * k + 2] = v.z;
+          w[4 * k + 3] = v.w;
+        }
+        tmem_st32(tmem + COL_Q + lane_off + 32 * c, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_tmem);
+    }
     for (int j = 0; j < n_kv && ok; ++j) {
       const int s = j & 1;
       if (j >= 2 && !wait_pv(j - 2)) {
@@ -229,6 +269,7 @@ __global__ void __launch_bounds__(192, 1)
         ok = false;
         break;
       }
+      if (lane == 0) LAGA_TRACE_POINT(fwd, 10, j);
       tc_fence_after();
       const uint32_t s_addr = tmem + s * 128 + lane_off;
       float x[128];
@@ -248,6 +289,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int i = 0; i < 128; ++i)
           if (kv0 + i > limit) x[i] = -INFINITY;
       }
+      if (lane == 0) LAGA_TRACE_POINT(fwd, 11, j);
       float mt = x[0];
 #pragma unroll
       for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
@@ -274,6 +316,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       l_run = l_run * alpha + sum;
       m_run = m_use;
+      if (lane == 0) LAGA_TRACE_POINT(fwd, 12, j);
       {
         uint32_t w[32];
 #pragma unroll
@@ -305,6 +348,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[s]);
+      if (lane == 0) LAGA_TRACE_POINT(fwd, 13, j);
     }
     if (ok && wait_pv(n_kv - 1)) {
       tc_fence_after();

@@ -263,3 +263,33 @@ __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* sta
   if (a != 0 && status != nullptr) atomicCAS(status, 0, a);
 }
 }  // namespace laga
+
+// ------------------------------------------------------------------ debug trace
+// Built only with -DLAGA_TRACE: kernels stamp the SM clock at chosen points of
+// one CTA (blockIdx 0) into a per-file device array, slot
+// (warp, step, tag), with plain stores; a debug export copies the array out.
+// Release builds compile every trace point to nothing.
+#ifdef LAGA_TRACE
+#define LAGA_TRACE_WARPS 16
+#define LAGA_TRACE_STEPS 512
+#define LAGA_TRACE_TAGS 32
+#define LAGA_TRACE_CAP (LAGA_TRACE_WARPS * LAGA_TRACE_STEPS * LAGA_TRACE_TAGS)
+#define LAGA_TRACE_DEFINE(name)                                                          \
+  __device__ long long g_trace_##name[LAGA_TRACE_CAP];                                  \
+  extern "C" int laga_debug_trace_##name(long long* host, int max) {                     \
+    const int n = max < LAGA_TRACE_CAP ? max : LAGA_TRACE_CAP;                           \
+    cudaMemcpyFromSymbol(host, g_trace_##name, n * sizeof(long long));                  \
+    return n;                                                                            \
+  }
+#define LAGA_TRACE_POINT(name, tag, step)                                                \
+  do {                                                                                   \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (step) < LAGA_TRACE_STEPS) \
+      g_trace_##name[((threadIdx.x >> 5) * LAGA_TRACE_STEPS + (step)) * LAGA_TRACE_TAGS + (tag)] = \
+          clock64();                                                                     \
+  } while (0)
+#else
+#define LAGA_TRACE_DEFINE(name)
+#define LAGA_TRACE_POINT(name, tag, step) \
+  do {                                    \
+  } while (0)
+#endif
