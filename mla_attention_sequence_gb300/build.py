@@ -43,7 +43,7 @@ def _flags(ptxas_verbose: bool):
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]
     if TRACE:
-        f += ["-DLAGA_TRACE"]
+        f += ["-DLAGA_TRACE", f"-DLAGA_TRACE_BY={int(os.environ.get('LAGA_TRACE_BY', '0'))}"]
     return f
 
 

@@ -23,6 +23,8 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+LAGA_TRACE_DEFINE(dkdv)
+
 namespace laga {
 namespace {
 
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
                          const __grid_constant__ CUtensorMap mdO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
+  LAGA_TRACE_CTA_BEGIN(dkdv);
+  LAGA_TRACE_POINT(dkdv, 30, 0);
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (; i < n_qt; ++i) {
         const int s = i % NSTAGE;
         if (!mbar_wait_or_abort(&q_empty[s], ((i / NSTAGE) & 1) ^ 1, abort_flag, 51)) break;
+        LAGA_TRACE_POINT(dkdv, 20, i);
         const int q0 = (first_qt + i) * BQ;
         uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
         float* rows = reinterpret_cast<float*>(smem + OFF_ROWV) + s * 2 * BQ;
@@ -160,85 +165,100 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait_or_abort(kv_full, 0, abort_flag, 52);
-      bool issued = false;
-      tc_fence_after();
-      const uint32_t k_base = smem_u32(smem + OFF_K);
-      const uint32_t v_base = smem_u32(smem + OFF_V);
-      auto stage = [&](int i) { return smem_u32(smem + OFF_STAGE + (i % NSTAGE) * STAGE_BYTES); };
-      auto wait_q = [&](int i) {
-        return mbar_wait_or_abort(&q_full[i % NSTAGE], (i / NSTAGE) & 1, abort_flag, 53);
-      };
-      auto issue_s = [&](int i) {  // S^T(i) = K Q_i^T
-        const uint32_t q_base = stage(i);
-        const uint32_t d = tmem + COL_S + 64u * (i & 1);
+    // The whole warp runs the issue loop (warp-uniform waits, elected lane issues).
+    bool ok = warp_wait_or_abort(kv_full, 0, abort_flag, 52);
+    bool issued = false;
+    tc_fence_after();
+    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+    // K-major (16) and MN-major (QBOX) descriptors of a stage's Q and dO tiles
+    auto stage_desc = [&](int i, uint32_t off, uint32_t lbo) {
+      return sdesc_sw128(smem_u32(smem + OFF_STAGE + (i % NSTAGE) * STAGE_BYTES + off), lbo, 1024);
+    };
+    auto wait_q = [&](int i) {
+      return warp_wait_or_abort(&q_full[i % NSTAGE], (i / NSTAGE) & 1, abort_flag, 53);
+    };
+    auto issue_s = [&](int i) {  // S^T(i) = K Q_i^T
+      const uint64_t q_desc = stage_desc(i, 0, 16);
+      const uint32_t d = tmem + COL_S + 64u * (i & 1);
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint32_t c = kk >> 2, k = kk & 3;
-          mma_ss(d, sdesc_sw128(k_base + c * KBOX + k * 32, 16, 1024),
-                 sdesc_sw128(q_base + c * QBOX + k * 32, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[i & 1]);
-      };
-      auto issue_dp = [&](int i) {  // dP^T(i) = V dO_i^T
-        const uint32_t do_base = stage(i) + Q_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t c = kk >> 2, k = kk & 3;
-          mma_ss(tmem + COL_DP, sdesc_sw128(v_base + c * KBOX + k * 32, 16, 1024),
-                 sdesc_sw128(do_base + c * QBOX + k * 32, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(dp_full);
-      };
-      if (ok && n_qt > 0) {
-        ok = wait_q(0);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-          issue_dp(0);
-          issued = true;
-        }
-        if (ok && n_qt > 1) {
-          ok = wait_q(1);
-          if (ok) {
-            tc_fence_after();
-            issue_s(1);
-          }
-        }
+      for (int kk = 0; kk < 12; ++kk) {
+        const uint32_t c = kk >> 2, k = kk & 3;
+        mma_ss_warp(d, k_desc + ((c * KBOX + k * 32) >> 4), q_desc + ((c * QBOX + k * 32) >> 4), IDESC_ST,
+                    kk > 0 ? 1u : 0u);
       }
-      for (int i = 0; i < n_qt && ok; ++i) {
-        const uint32_t q_base = stage(i);
-        const uint32_t do_base = q_base + Q_BYTES;
-        if (!mbar_wait_or_abort(&p_full[i & 1], (i >> 1) & 1, abort_flag, 54)) { ok = false; break; }
-        tc_fence_after();
-        // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
-        const uint32_t pt = tmem + COL_S + 64u * (i & 1);
+      mma_commit_warp(&s_full[i & 1]);
+    };
+    auto issue_dp = [&](int i) {  // dP^T(i) = V dO_i^T
+      const uint64_t do_desc = stage_desc(i, Q_BYTES, 16);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + COL_DV, pt + packed_col(k), sdesc_sw128(do_base + k * 2048, QBOX, 1024), IDESC_DV,
-                 (i > 0 || k > 0) ? 1u : 0u);
-        if (!mbar_wait_or_abort(ds_full, i & 1, abort_flag, 55)) { ok = false; break; }
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t c = kk >> 2, k = kk & 3;
+        mma_ss_warp(tmem + COL_DP, v_desc + ((c * KBOX + k * 32) >> 4), do_desc + ((c * QBOX + k * 32) >> 4),
+                    IDESC_ST, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_warp(dp_full);
+    };
+    // Each barrier is tested (without blocking) before the MMA group that precedes
+    // its use, so the check after that group costs no shared-memory round trip
+    // behind the MMAs.
+    uint32_t tp = 0;
+    if (ok && n_qt > 0) {
+      ok = wait_q(0);
+      if (ok) {
         tc_fence_after();
-        // dK += dS^T Q_i : all 192 head dims in one product
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + COL_DK, tmem + COL_DP + packed_col(k), sdesc_sw128(q_base + k * 2048, QBOX, 1024), IDESC_DK,
-                 (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&q_empty[i % NSTAGE]);
-        if (i + 1 < n_qt) issue_dp(i + 1);
-        if (i + 2 < n_qt) {
-          if (!wait_q(i + 2)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(i + 2);
-        }
+        issue_s(0);
+        issue_dp(0);
+        issued = true;
+        if (n_qt > 1) ok = wait_q(1);
       }
       if (ok) {
-        mma_commit(acc_done);
-      } else if (issued) {
-        mma_commit(drain);
-        mbar_drain(drain, 0);
+        tp = mbar_test(&p_full[0], 0);
+        if (n_qt > 1) {
+          tc_fence_after();
+          issue_s(1);
+        }
       }
+    }
+    for (int i = 0; i < n_qt && ok; ++i) {
+      if (!warp_wait_token(&p_full[i & 1], (i >> 1) & 1, tp, abort_flag, 54)) { ok = false; break; }
+      const uint32_t td = mbar_test(ds_full, i & 1);
+      tc_fence_after();
+      // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
+      const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
+      const uint32_t pt = tmem + COL_S + 64u * (i & 1);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ts_warp(tmem + COL_DV, pt + packed_col(k), do_mn + ((k * 2048) >> 4), IDESC_DV, (i > 0 || k > 0) ? 1u : 0u);
+      if (!warp_wait_token(ds_full, i & 1, td, abort_flag, 55)) { ok = false; break; }
+      const uint32_t tq = i + 2 < n_qt ? mbar_test(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1) : 1u;
+      tc_fence_after();
+      // dK += dS^T Q_i : all 192 head dims in one product
+      const uint64_t q_mn = stage_desc(i, 0, QBOX);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ts_warp(tmem + COL_DK, tmem + COL_DP + packed_col(k), q_mn + ((k * 2048) >> 4), IDESC_DK,
+                    (i > 0 || k > 0) ? 1u : 0u);
+      mma_commit_warp(&q_empty[i % NSTAGE]);
+      if (i + 1 < n_qt) issue_dp(i + 1);
+      if (i + 2 < n_qt) {
+        if (!warp_wait_token(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, tq, abort_flag, 53)) {
+          ok = false;
+          break;
+        }
+        tp = mbar_test(&p_full[(i + 1) & 1], ((i + 1) >> 1) & 1);
+        tc_fence_after();
+        issue_s(i + 2);
+      } else {
+        tp = 0;  // no group left to hide the test behind: wait in full
+      }
+    }
+    if (ok) {
+      mma_commit_warp(acc_done);
+    } else if (issued) {
+      mma_commit_warp(drain);
+      if (lane == 0) mbar_drain(drain, 0);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------ key-row warps
@@ -262,6 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int qc = (first_qt + i) * BQ + 32 * half;  // this thread's first query column
       if (!warp_wait(&q_full[s], (i / NSTAGE) & 1, 61)) { ok = false; break; }
       if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, 62)) { ok = false; break; }
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 10, i);
       tc_fence_after();
       const float* lse = reinterpret_cast<const float*>(smem + OFF_ROWV) + s * 2 * BQ + 32 * half;
       const float* dlt = lse + BQ;
@@ -292,7 +313,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 11, i);
       if (!warp_wait(dp_full, i & 1, 63)) { ok = false; break; }
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 12, i);
       tc_fence_after();
       const uint32_t dp_addr = tmem + COL_DP + lane_off;
       {
@@ -310,8 +333,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 13, i);
     }
     if (ok && warp_wait(acc_done, 0, 64)) {
+      LAGA_TRACE_POINT(dkdv, 29, 0);
       tc_fence_after();
       const long long row = static_cast<long long>(b) * p.skv_pad + kv;
       const long long ncol = static_cast<long long>(p.n_h) * 128;
@@ -349,9 +374,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  LAGA_TRACE_POINT(dkdv, 28, 0);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) publish_abort(abort_flag, p.status);
+  LAGA_TRACE_POINT(dkdv, 31, 0);
+  LAGA_TRACE_CTA_END(dkdv);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);

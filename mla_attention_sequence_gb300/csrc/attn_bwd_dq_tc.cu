@@ -12,17 +12,21 @@
 // the forward: S = Q_nope K_nope^T + Q_rope k_rope^T, and dq's last 64 columns
 // come from the k_rope tile.
 //
-// Warp roles (320 threads):
-//   warp 0      lane 0: TMA for Q and dO once, then key tiles; lane 1: value tiles
+// Warp roles (352 threads):
+//   warp 0      lane 0: TMA for Q and dO once, then key tiles
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
 //   warps 2..9  two warpgroups; each thread owns one query row (TMEM lane) and
 //               half of the tile's 64 key columns: P, dS, and half the epilogue
+//   warp 10     lane 0: TMA for value tiles (its own warp, so that its waits
+//               never hold back the key-tile producer)
 // TMEM columns: S/dS x2 [0,128), dP x2 [128,256), dq [256,448), dO [448,512).
 // dO is the same for every key tile: the query-row warps copy it into TMEM
 // once and dP = dO V^T reads it from there (A operand from TMEM), which takes
 // its reads off the shared-memory port that bounds this kernel.
 #include "internal.h"
 #include "ptx.cuh"
+
+LAGA_TRACE_DEFINE(dq)
 
 namespace laga {
 namespace {
@@ -46,7 +50,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DO = 448;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
 constexpr uint32_t IDESC_DQ = idesc_bf16(128, 192, false, true);
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 352;
 constexpr uint32_t SOFTMAX_WARPS = 8;
 
 struct Params {
@@ -72,6 +76,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
                        const __grid_constant__ CUtensorMap mdO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
+  LAGA_TRACE_CTA_BEGIN(dq);
+  LAGA_TRACE_POINT(dq, 30, 0);
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
@@ -151,7 +157,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = j - NSTAGE < 0 ? 0 : j - NSTAGE; i < j; ++i)
           mbar_drain(&k_full[i % NSTAGE], (i / NSTAGE) & 1);
       }
-    } else if (lane == 1) {
+    }
+  } else if (warp == 10) {
+    if (lane == 0) {
       tma_prefetch_desc(&mV);
       int j = 0;
       for (; j < n_kv; ++j) {
@@ -168,62 +176,87 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mbar_drain(&v_full[i % NSTAGE], (i / NSTAGE) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait_or_abort(q_full, 0, abort_flag, 73) && mbar_wait_or_abort(do_tmem, 0, abort_flag, 77);
-      bool issued = false;
-      tc_fence_after();
-      const uint32_t q_base = smem_u32(smem + OFF_Q);
-      auto issue_s_dp = [&](int j) -> bool {  // S(j) = Q K_j^T ; dP(j) = dO V_j^T
-        const int s = j % NSTAGE;
-        const uint32_t ph = (j / NSTAGE) & 1;
-        if (!mbar_wait_or_abort(&k_full[s], ph, abort_flag, 74)) return false;
-        tc_fence_after();
-        const uint32_t k_base = smem_u32(smem + OFF_K + s * K_BYTES);
-        const uint32_t ds = tmem + COL_S + 64u * (j & 1);
+    // The whole warp runs the issue loop; an elected lane issues. Each barrier is
+    // tested (without blocking) before the MMA group that precedes its use, so the
+    // check after that group costs no shared-memory round trip behind the MMAs.
+    bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 73) && warp_wait_or_abort(do_tmem, 0, abort_flag, 77);
+    bool issued = false;
+    tc_fence_after();
+    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+    auto issue_s = [&](int j) {  // S(j) = Q K_j^T
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + OFF_K + (j % NSTAGE) * K_BYTES), 16, 1024);
+      const uint32_t ds = tmem + COL_S + 64u * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint32_t c = kk >> 2, k = kk & 3;
-          mma_ss(ds, sdesc_sw128(q_base + c * QBOX + k * 32, 16, 1024),
-                 sdesc_sw128(k_base + c * KBOX + k * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        if (!mbar_wait_or_abort(&v_full[s], ph, abort_flag, 75)) return false;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(smem + OFF_V + s * V_BYTES);
-        const uint32_t dd = tmem + COL_DP + 64u * (j & 1);
+      for (int kk = 0; kk < 12; ++kk) {
+        const uint32_t c = kk >> 2, k = kk & 3;
+        mma_ss_warp(ds, q_desc + ((c * QBOX + k * 32) >> 4), k_desc + ((c * KBOX + k * 32) >> 4), IDESC_S,
+                    kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T, then S(j) and dP(j) are announced
+      const int s = j % NSTAGE;
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V + s * V_BYTES), 16, 1024);
+      const uint32_t dd = tmem + COL_DP + 64u * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // head dims [16kk, 16kk + 16): dO columns [8kk, 8kk + 8)
-          const uint32_t c = kk >> 2, k = kk & 3;
-          mma_ts(dd, tmem + COL_DO + kk * 8, sdesc_sw128(v_base + c * KBOX + k * 32, 16, 1024), IDESC_S,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[j & 1]);
-        mma_commit(&v_empty[s]);
-        return true;
-      };
+      for (int kk = 0; kk < 8; ++kk)  // head dims [16kk, 16kk + 16): dO columns [8kk, 8kk + 8)
+        mma_ts_warp(dd, tmem + COL_DO + kk * 8, v_desc + (((kk >> 2) * KBOX + (kk & 3) * 32) >> 4), IDESC_S,
+                    kk > 0 ? 1u : 0u);
+      mma_commit_warp(&s_full[j & 1]);
+      mma_commit_warp(&v_empty[s]);
+    };
+    auto issue_dq = [&](int j) {  // dq += dS(j) K_j : A = dS (TMEM, packed bf16), B = key tile MN-major (N = 192)
+      const int s = j % NSTAGE;
+      const uint64_t k_mn = sdesc_sw128(smem_u32(smem + OFF_K + s * K_BYTES), KBOX, 1024);
+      const uint32_t ds = tmem + COL_S + 64u * (j & 1);
+#pragma unroll
+      for (int k = 0; k < BKV / 16; ++k)
+        mma_ts_warp(tmem + COL_DQ, ds + packed_col(k), k_mn + ((k * 2048) >> 4), IDESC_DQ, (j > 0 || k > 0) ? 1u : 0u);
+      mma_commit_warp(&k_empty[s]);
+    };
+    uint32_t tk = 0;
+    if (ok) {
+      ok = warp_wait_or_abort(&k_full[0], 0, abort_flag, 74);
       if (ok) {
-        ok = issue_s_dp(0);
+        const uint32_t tv = mbar_test(&v_full[0], 0);
+        tc_fence_after();
+        issue_s(0);
         issued = true;
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !issue_s_dp(j + 1)) { ok = false; break; }
-        if (!mbar_wait_or_abort(&ds_full[j & 1], (j >> 1) & 1, abort_flag, 76)) { ok = false; break; }
-        tc_fence_after();
-        // dq += dS(j) K_j : A = dS (TMEM, packed bf16), B = key tile read MN-major (N = 192)
-        const int s = j % NSTAGE;
-        const uint32_t k_base = smem_u32(smem + OFF_K + s * K_BYTES);
-        const uint32_t ds = tmem + COL_S + 64u * (j & 1);
-#pragma unroll
-        for (int k = 0; k < BKV / 16; ++k)
-          mma_ts(tmem + COL_DQ, ds + packed_col(k), sdesc_sw128(k_base + k * 2048, KBOX, 1024), IDESC_DQ,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&k_empty[s]);
+        ok = warp_wait_token(&v_full[0], 0, tv, abort_flag, 75);
       }
       if (ok) {
-        mma_commit(dq_done);
-      } else if (issued) {
-        mma_commit(drain);
-        mbar_drain(drain, 0);
+        tk = n_kv > 1 ? mbar_test(&k_full[1 % NSTAGE], (1 / NSTAGE) & 1) : 1u;
+        tc_fence_after();
+        issue_dp(0);
       }
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const uint32_t dph = (j >> 1) & 1;
+      uint32_t td;
+      if (j + 1 < n_kv) {  // S(j+1) and dP(j+1) go ahead of dq(j): softmax of j+1 overlaps dq(j)
+        const int jn = j + 1, sn = jn % NSTAGE;
+        const uint32_t pn = (jn / NSTAGE) & 1;
+        if (!warp_wait_token(&k_full[sn], pn, tk, abort_flag, 74)) { ok = false; break; }
+        const uint32_t tv = mbar_test(&v_full[sn], pn);
+        tc_fence_after();
+        issue_s(jn);
+        if (!warp_wait_token(&v_full[sn], pn, tv, abort_flag, 75)) { ok = false; break; }
+        td = mbar_test(&ds_full[j & 1], dph);
+        tc_fence_after();
+        issue_dp(jn);
+      } else {
+        td = mbar_test(&ds_full[j & 1], dph);
+      }
+      if (!warp_wait_token(&ds_full[j & 1], dph, td, abort_flag, 76)) { ok = false; break; }
+      tk = j + 2 < n_kv ? mbar_test(&k_full[(j + 2) % NSTAGE], ((j + 2) / NSTAGE) & 1) : 1u;
+      tc_fence_after();
+      issue_dq(j);
+    }
+    if (ok) {
+      mma_commit_warp(dq_done);
+    } else if (issued) {
+      mma_commit_warp(drain);
+      if (lane == 0) mbar_drain(drain, 0);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------ query-row warps
@@ -266,6 +299,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int j = 0; j < n_kv && ok; ++j) {
       if (!warp_wait(&s_full[j & 1], (j >> 1) & 1, 81)) { ok = false; break; }
+      if (lane == 0) LAGA_TRACE_POINT(dq, 10, j);
       tc_fence_after();
       const uint32_t s_addr = tmem + COL_S + 64u * (j & 1) + lane_off;
       const uint32_t dp_addr = tmem + COL_DP + 64u * (j & 1) + lane_off;
@@ -297,8 +331,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[j & 1]);
+      if (lane == 0) LAGA_TRACE_POINT(dq, 11, j);
     }
     if (ok && warp_wait(dq_done, 0, 82)) {
+      LAGA_TRACE_POINT(dq, 29, 0);
       tc_fence_after();
       const bool valid = q_row < p.Sq;
       bf16* dst = p.dq + ((static_cast<long long>(b) * p.Sq + q_row) * p.n_h + h) * 192;
@@ -323,9 +359,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  LAGA_TRACE_POINT(dq, 28, 0);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) publish_abort(abort_flag, p.status);
+  LAGA_TRACE_POINT(dq, 31, 0);
+  LAGA_TRACE_CTA_END(dq);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);

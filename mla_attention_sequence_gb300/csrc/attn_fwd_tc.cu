@@ -6,17 +6,23 @@
 // S = Q K^T is the sum of the no-RoPE product (K = 128) and the RoPE product
 // against the shared k_rope tile (K = 64), accumulated into one TMEM tile.
 //
-// Warp roles (192 threads):
-//   warp 0      lane 0: TMA for Q and K tiles; lane 1: TMA for V tiles
+// Warp roles (224 threads):
+//   warp 0      lane 0: TMA for K tiles (3-stage ring)
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
 //   warps 2..5  softmax: one query row per thread (TMEM lane), online max and
 //               sum in the log2 domain, P written back over S as bf16 pairs,
 //               O rescaled in TMEM when the running max grows, final epilogue
+//   warp 6      lane 0: TMA for V tiles
+// The two TMA producers sit in different warps: as two lanes of one warp their
+// loops diverge, and a lane blocked waiting for a free slot holds back the other
+// lane's copies.
 // TMEM columns: S/P buffer 0 [0,128), S/P buffer 1 [128,256), O [256,384),
-// Q [384,480). Q is the same for every key tile, so the softmax warps copy it
-// into TMEM once and S = Q K^T reads it from there (A operand from TMEM): the
-// shared-memory port then only carries K for S, V for PV and the TMA writes,
-// which is what bounds this kernel.
+// Q [384,480). Q is the same for every key tile, so each softmax thread loads
+// its query row from global memory straight into TMEM once and S = Q K^T reads
+// it from there (A operand from TMEM). Q never occupies shared memory, which
+// leaves room for a third K stage: a 48 KB K tile takes longer to arrive under
+// full load than one key-tile step lasts, and two stages left the MMA issuer
+// waiting for K at every step.
 // MMA order S(0), S(1), PV(0), S(2), PV(1), ... lets softmax of tile j+1
 // overlap the PV product of tile j.
 #include "internal.h"
@@ -30,10 +36,18 @@ namespace {
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int BOX = 16384;  // one [128 rows][64 cols] bf16 box
-constexpr int Q_BYTES = 3 * BOX;
 constexpr int K_BYTES = 3 * BOX;
 constexpr int V_BYTES = 2 * BOX;
-constexpr int SMEM_BYTES = Q_BYTES + 2 * K_BYTES + 2 * V_BYTES + 1024 + 256;
+constexpr int K_STAGES = 3;
+// K/V tiles are prefetched into L2 this many tiles ahead of their TMA load.
+constexpr int PREFETCH = 4;
+constexpr int V_STAGES = 2;
+constexpr int SMEM_BYTES = K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
+#ifdef LAGA_TRACE
+constexpr int NTHREADS = 288;  // warps 7 and 8 stamp K and V tile arrivals
+#else
+constexpr int NTHREADS = 224;
+#endif
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
 constexpr uint32_t COL_Q = 384;
@@ -49,6 +63,7 @@ struct FwdParams {
   int* status;  // device status word (timeouts)
   int Sq, S, n_h, q_offset, causal, skv_pad, n_q_tiles;
   float scale_log2;  // softmax scale * log2(e)
+  const bf16* q;     // [B][Sq][n_h][192]
   bf16* out;
   float* lse;
 };
@@ -58,28 +73,27 @@ __device__ __forceinline__ int n_kv_tiles(const FwdParams& p, int t) {
   return last / BKV + 1;
 }
 
-__global__ void __launch_bounds__(192, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                    const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
-                    const FwdParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mR,
+                    const __grid_constant__ CUtensorMap mV, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
+  LAGA_TRACE_CTA_BEGIN(fwd);
+  LAGA_TRACE_POINT(fwd, 30, 0);
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + Q_BYTES;
-  uint8_t* sV = sK + 2 * K_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * V_BYTES);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]
-  uint64_t* p_full = bars + 11;  // [2]
-  uint64_t* pv_done = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint64_t* q_tmem = bars + 15;  // Q copied into TMEM by the softmax warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + K_STAGES * K_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + V_STAGES * V_BYTES);
+  uint64_t* k_full = bars + 0;   // [K_STAGES]
+  uint64_t* k_empty = bars + 3;  // [K_STAGES]
+  uint64_t* v_full = bars + 6;   // [V_STAGES]
+  uint64_t* v_empty = bars + 8;  // [V_STAGES]
+  uint64_t* s_full = bars + 10;  // [2]
+  uint64_t* p_full = bars + 12;  // [2]
+  uint64_t* pv_done = bars + 14;
+  uint64_t* drain = bars + 15;
+  uint64_t* q_tmem = bars + 16;  // Q written into TMEM by the softmax warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -91,10 +105,11 @@ __global__ void __launch_bounds__(192, 1)
   const int n_kv = n_kv_tiles(p, t);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < K_STAGES; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
@@ -117,18 +132,12 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mR);
-      mbar_arrive_expect_tx(q_full, Q_BYTES);
-      const int qc = h * 192;
-      tma_load_3d(sQ, &mQ, q_full, qc, t * BQ, b);
-      tma_load_3d(sQ + BOX, &mQ, q_full, qc + 64, t * BQ, b);
-      tma_load_3d(sQ + 2 * BOX, &mQ, q_full, qc + 128, t * BQ, b);
       int j = 0;
       for (; j < n_kv; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_or_abort(&k_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, 11)) break;
+        const int s = j % K_STAGES;
+        if (!mbar_wait_or_abort(&k_empty[s], ((j / K_STAGES) & 1) ^ 1, abort_flag, 11)) break;
         LAGA_TRACE_POINT(fwd, 20, j);
         uint8_t* dst = sK + s * K_BYTES;
         mbar_arrive_expect_tx(&k_full[s], K_BYTES);
@@ -136,12 +145,17 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(dst, &mK, &k_full[s], h * 128, row);
         tma_load_2d(dst + BOX, &mK, &k_full[s], h * 128 + 64, row);
         tma_load_3d(dst + 2 * BOX, &mR, &k_full[s], 0, j * BKV, b);
+        if (j + PREFETCH < n_kv) {
+          tma_prefetch_2d(&mK, h * 128, row + PREFETCH * BKV);
+          tma_prefetch_2d(&mK, h * 128 + 64, row + PREFETCH * BKV);
+        }
       }
-      if (j < n_kv) {  // aborted: let issued copies land
-        mbar_drain(q_full, 0);
-        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&k_full[i & 1], (i >> 1) & 1);
-      }
-    } else if (lane == 1) {
+      if (j < n_kv)  // aborted: let issued copies land
+        for (int i = j - K_STAGES < 0 ? 0 : j - K_STAGES; i < j; ++i)
+          mbar_drain(&k_full[i % K_STAGES], (i / K_STAGES) & 1);
+    }
+  } else if (warp == 6) {
+    if (lane == 0) {
       tma_prefetch_desc(&mV);
       int j = 0;
       for (; j < n_kv; ++j) {
@@ -153,62 +167,93 @@ __global__ void __launch_bounds__(192, 1)
         const int row = b * p.skv_pad + j * BKV;
         tma_load_2d(dst, &mV, &v_full[s], h * 128, row);
         tma_load_2d(dst + BOX, &mV, &v_full[s], h * 128 + 64, row);
+        if (j + PREFETCH < n_kv) {
+          tma_prefetch_2d(&mV, h * 128, row + PREFETCH * BKV);
+          tma_prefetch_2d(&mV, h * 128 + 64, row + PREFETCH * BKV);
+        }
       }
       if (j < n_kv)
         for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&v_full[i & 1], (i >> 1) & 1);
     }
-  } else if (warp == 1) {
+#ifdef LAGA_TRACE
+  } else if (warp == 7 || warp == 8) {
     if (lane == 0) {
-      bool ok = mbar_wait_or_abort(q_tmem, 0, abort_flag, 13);
-      bool issued = false;
-      tc_fence_after();
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj & 1;
-        const uint32_t ph = (jj >> 1) & 1;
-        if (!mbar_wait_or_abort(&p_full[s], ph, abort_flag, 14)) return false;
-        LAGA_TRACE_POINT(fwd, 3, jj);
-        if (!mbar_wait_or_abort(&v_full[s], ph, abort_flag, 15)) return false;
-        LAGA_TRACE_POINT(fwd, 4, jj);
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(sV + s * V_BYTES);
-        const uint32_t p_tmem = tmem + s * 128;
+      for (int j = 0; j < n_kv; ++j) {
+        uint64_t* bar = warp == 7 ? &k_full[j % K_STAGES] : &v_full[j & 1];
+        const uint32_t ph = warp == 7 ? (j / K_STAGES) & 1 : (j >> 1) & 1;
+        if (!mbar_wait_or_abort(bar, ph, abort_flag, 30)) break;
+        LAGA_TRACE_POINT(fwd, warp == 7 ? 22 : 23, j);
+      }
+    }
+#endif
+  } else if (warp == 1) {
+    // The whole warp runs the issue loop; an elected lane issues. Each barrier is
+    // tested (without blocking) before the MMA group that precedes its use, so the
+    // check after that group costs no shared-memory round trip behind the MMAs.
+    bool ok = warp_wait_or_abort(q_tmem, 0, abort_flag, 13);
+    bool issued = false;
+    tc_fence_after();
+    auto issue_pv = [&](int jj) {
+      const int s = jj & 1;
+      const uint64_t v_desc = sdesc_sw128(smem_u32(sV + s * V_BYTES), BOX, 1024);
+      const uint32_t p_tmem = tmem + s * 128;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(v_base + kk * 2048, BOX, 1024);
-          mma_ts(tmem + COL_O, p_tmem + kk * 8, bd, IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(pv_done);
-        mma_commit(&v_empty[s]);
-        LAGA_TRACE_POINT(fwd, 5, jj);
-        return true;
-      };
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_or_abort(&k_full[s], (j >> 1) & 1, abort_flag, 16)) {
+      for (int kk = 0; kk < BKV / 16; ++kk)
+        mma_ts_warp(tmem + COL_O, p_tmem + kk * 8, v_desc + ((kk * 2048) >> 4), IDESC_PV,
+                    (jj > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_warp(pv_done);
+      mma_commit_warp(&v_empty[s]);
+    };
+    uint32_t tk = 0, tp = 0, tv = 0;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int s = j & 1;
+      const int ks = j % K_STAGES;
+      if (!warp_wait_token(&k_full[ks], (j / K_STAGES) & 1, tk, abort_flag, 16)) {
+        ok = false;
+        break;
+      }
+      if (j >= 1) {
+        tp = mbar_test(&p_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        tv = mbar_test(&v_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
+      }
+      tc_fence_after();
+      const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
+      const uint32_t d_tmem = tmem + s * 128;
+#pragma unroll
+      for (int kk = 0; kk < 12; ++kk)  // head dims [16kk, 16kk + 16): Q columns [8kk, 8kk + 8)
+        mma_ts_warp(d_tmem, tmem + COL_Q + kk * 8, k_desc + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4), IDESC_S,
+                    kk > 0 ? 1u : 0u);
+      issued = true;
+      mma_commit_warp(&s_full[s]);
+      mma_commit_warp(&k_empty[ks]);
+      if (j >= 1) {
+        const uint32_t ph = ((j - 1) >> 1) & 1;
+        if (!warp_wait_token(&p_full[(j - 1) & 1], ph, tp, abort_flag, 14) ||
+            !warp_wait_token(&v_full[(j - 1) & 1], ph, tv, abort_flag, 15)) {
           ok = false;
           break;
         }
-        LAGA_TRACE_POINT(fwd, 1, j);
+        tk = j + 1 < n_kv ? mbar_test(&k_full[(j + 1) % K_STAGES], ((j + 1) / K_STAGES) & 1) : 1u;
         tc_fence_after();
-        const uint32_t k_base = smem_u32(sK + s * K_BYTES);
-        const uint32_t d_tmem = tmem + s * 128;
-#pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {  // head dims [16kk, 16kk + 16): Q columns [8kk, 8kk + 8)
-          const uint32_t c = kk >> 2, k = kk & 3;
-          const uint64_t bd = sdesc_sw128(k_base + c * BOX + k * 32, 16, 1024);
-          mma_ts(d_tmem, tmem + COL_Q + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        issued = true;
-        mma_commit(&s_full[s]);
-        mma_commit(&k_empty[s]);
-        LAGA_TRACE_POINT(fwd, 2, j);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        issue_pv(j - 1);
+      } else {
+        tk = 0;
       }
-      if (ok) ok = issue_pv(n_kv - 1);
-      if (!ok && issued) {
-        mma_commit(drain);
-        mbar_drain(drain, 0);
+    }
+    if (ok) {
+      const int jl = n_kv - 1;
+      const uint32_t ph = (jl >> 1) & 1;
+      ok = warp_wait_or_abort(&p_full[jl & 1], ph, abort_flag, 14) &&
+           warp_wait_or_abort(&v_full[jl & 1], ph, abort_flag, 15);
+      if (ok) {
+        tc_fence_after();
+        issue_pv(jl);
       }
+    }
+    if (!ok && issued) {
+      mma_commit_warp(drain);
+      if (lane == 0) mbar_drain(drain, 0);
+      __syncwarp();
     }
   } else {
     // ---------------- softmax warpgroup: thread owns query row r of the tile
@@ -236,17 +281,17 @@ __global__ void __launch_bounds__(192, 1)
       return true;
     };
     // Q row r -> TMEM lane r as packed bf16 pairs (the A-operand layout of a
-    // TS-MMA): 16-byte chunk k of box c sits at row r of the 128-byte-swizzled
-    // tile the TMA wrote, and becomes TMEM columns [32c + 4k, 32c + 4k + 4).
-    if (!warp_wait(q_full, 0, 20)) ok = false;
-    if (ok) {
+    // TS-MMA): head dims 2i, 2i+1 become TMEM column i. Rows past Sq are zero.
+    {
+      const bool valid = q_row < p.Sq;
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          p.q + ((static_cast<long long>(b) * p.Sq + (valid ? q_row : 0)) * p.n_h + h) * 192);
 #pragma unroll 1
       for (int c = 0; c < 3; ++c) {
         uint32_t w[32];
-        const uint8_t* box = sQ + c * BOX;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 v = *reinterpret_cast<const uint4*>(box + sw128_offset(r, k));
+          const uint4 v = valid ? __ldg(qrow + 8 * c + k) : make_uint4(0u, 0u, 0u, 0u);
           w[4 * k + 0] = v.x;
           w[4 * k + 1] = v.y;
           w[4 * k + 2] = v.z;
@@ -351,6 +396,7 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) LAGA_TRACE_POINT(fwd, 13, j);
     }
     if (ok && wait_pv(n_kv - 1)) {
+      LAGA_TRACE_POINT(fwd, 29, 0);
       tc_fence_after();
       const uint32_t o_addr = tmem + COL_O + lane_off;
       const bool valid = q_row < p.Sq;
@@ -380,9 +426,12 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  LAGA_TRACE_POINT(fwd, 28, 0);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) publish_abort(abort_flag, p.status);
+  LAGA_TRACE_POINT(fwd, 31, 0);
+  LAGA_TRACE_CTA_END(fwd);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -391,22 +440,15 @@ __global__ void __launch_bounds__(192, 1)
 
 }  // namespace
 
-// The [rows][64] boxes of the operands: 3D q map over [B][Sq][n_h*192], 2D maps
-// over the [B*skv_pad][n_h*128] K/V workspace, 3D k_rope map over [B][S][64].
+// The [rows][64] boxes of the operands: 2D maps over the [B*skv_pad][n_h*128]
+// K/V workspace, 3D k_rope map over [B][S][64]. q is read row by row.
 LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const bf16* v_ws, const bf16* k_rope,
                          bf16* out, float* lse, cudaStream_t st) {
   LaunchResult r;
-  CUtensorMap mQ, mK, mR, mV;
-  {
-    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 192;
-    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
-    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
-    const uint32_t box[3] = {64, 128, 1};
-    r.cu = make_tmap(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-  }
+  CUtensorMap mK, mR, mV;
   const uint64_t kv_inner = static_cast<uint64_t>(d.n_h) * 128;
   const uint64_t kv_rows = static_cast<uint64_t>(d.B) * d.skv_pad;
-  if (r.cu == CUDA_SUCCESS) {
+  {
     const uint64_t dims[2] = {kv_inner, kv_rows};
     const uint64_t strides[1] = {kv_inner * 2};
     const uint32_t box[2] = {64, 128};
@@ -434,6 +476,7 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
   p.skv_pad = d.skv_pad;
   p.n_q_tiles = (d.Sq + BQ - 1) / BQ;
   p.scale_log2 = d.scale * LOG2E;
+  p.q = q;
   p.out = out;
   p.lse = lse;
   p.status = device_status_ptr();
@@ -442,7 +485,7 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
     r.what = "cudaFuncSetAttribute(attn_fwd)";
     return r;
   }
-  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), 192, SMEM_BYTES, st>>>(mQ, mK, mR, mV, p);
+  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mK, mR, mV, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_fwd_kernel launch";
   return r;

@@ -76,6 +76,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// L2 prefetch of one tensor-map box (no shared memory, no completion signal):
+// warms L2 for a box that a later cp.async.bulk.tensor load will read.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
+}
+
 // Plain (non-tensor) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -150,6 +163,42 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective forms: every lane of a converged warp executes them and one
+// lane (elect.sync) issues the instruction. Keeping the issuing loop warp-uniform
+// lets descriptor arithmetic stay on the uniform datapath; a single lane running
+// the loop alone issues MMAs markedly slower once softmax warps share its
+// sub-partition.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 
@@ -257,6 +306,43 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 }  // namespace laga
 
 namespace laga {
+// Warp-uniform bounded wait: lane 0 waits, every lane gets its verdict.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int where) {
+  bool w = true;
+  if ((threadIdx.x & 31) == 0) w = mbar_wait_or_abort(bar, parity, abort_flag, where);
+  const bool all = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+  __syncwarp();  // order lane 0's acquire before the other lanes' reads
+  return all;
+}
+
+// Non-blocking test of an mbarrier phase (acquire on success). Meant to be issued
+// by the MMA warp BEFORE a group of tcgen05.mma: a shared-memory access issued
+// right after such a group waits behind it for well over 100 cycles, and a branch
+// on its result leaves the tensor pipe idle for that long. The result is then
+// consumed as a token by warp_wait_token after the group.
+__device__ __forceinline__ uint32_t mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// Warp-collective wait for a phase this lane already tested (token = that test's
+// result): with a set token no memory is touched. The verdict is made uniform
+// across the warp.
+__device__ __forceinline__ bool warp_wait_token(uint64_t* bar, uint32_t parity, uint32_t token,
+                                                volatile int* abort_flag, int where) {
+  bool ok = true;
+  if (!token) ok = mbar_wait_or_abort(bar, parity, abort_flag, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Called by one thread after the CTA's final barrier: publish an abort.
 __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* status) {
   const int a = *abort_flag;
@@ -274,22 +360,61 @@ __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* sta
 #define LAGA_TRACE_STEPS 512
 #define LAGA_TRACE_TAGS 32
 #define LAGA_TRACE_CAP (LAGA_TRACE_WARPS * LAGA_TRACE_STEPS * LAGA_TRACE_TAGS)
+#define LAGA_TRACE_CTAS 32768
+#ifndef LAGA_TRACE_BY
+#define LAGA_TRACE_BY 0  // blockIdx.y of the CTA whose steps are stamped
+#endif
 #define LAGA_TRACE_DEFINE(name)                                                          \
   __device__ long long g_trace_##name[LAGA_TRACE_CAP];                                  \
+  __device__ long long g_cta_##name[LAGA_TRACE_CTAS * 8];                               \
   extern "C" int laga_debug_trace_##name(long long* host, int max) {                     \
     const int n = max < LAGA_TRACE_CAP ? max : LAGA_TRACE_CAP;                           \
     cudaMemcpyFromSymbol(host, g_trace_##name, n * sizeof(long long));                  \
     return n;                                                                            \
+  }                                                                                      \
+  extern "C" int laga_debug_cta_##name(long long* host, int max) {                       \
+    const int n = max < LAGA_TRACE_CTAS * 8 ? max : LAGA_TRACE_CTAS * 8;                 \
+    cudaMemcpyFromSymbol(host, g_cta_##name, n * sizeof(long long));                    \
+    return n;                                                                            \
   }
 #define LAGA_TRACE_POINT(name, tag, step)                                                \
   do {                                                                                   \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (step) < LAGA_TRACE_STEPS) \
+    if (blockIdx.x == 0 && blockIdx.y == LAGA_TRACE_BY && blockIdx.z == 0 && (step) < LAGA_TRACE_STEPS) \
       g_trace_##name[((threadIdx.x >> 5) * LAGA_TRACE_STEPS + (step)) * LAGA_TRACE_TAGS + (tag)] = \
           clock64();                                                                     \
+  } while (0)
+// Per-CTA record (linear block index, SM id, entry and exit global time in ns,
+// entry and exit SM clock), written by thread 0 at kernel entry (BEGIN) and
+// after the final barrier (END).
+#define LAGA_TRACE_CTA_BEGIN(name)                                                       \
+  do {                                                                                   \
+    const long long cta_ = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z); \
+    if (threadIdx.x == 0 && cta_ < LAGA_TRACE_CTAS) {                                    \
+      uint32_t smid_;                                                                    \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));                                 \
+      g_cta_##name[cta_ * 8 + 0] = cta_;                                                 \
+      g_cta_##name[cta_ * 8 + 1] = smid_;                                                \
+      g_cta_##name[cta_ * 8 + 2] = (long long)global_ns();                               \
+      g_cta_##name[cta_ * 8 + 4] = clock64();                                            \
+    }                                                                                    \
+  } while (0)
+#define LAGA_TRACE_CTA_END(name)                                                         \
+  do {                                                                                   \
+    const long long cta_ = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z); \
+    if (threadIdx.x == 0 && cta_ < LAGA_TRACE_CTAS) {                                    \
+      g_cta_##name[cta_ * 8 + 3] = (long long)global_ns();                               \
+      g_cta_##name[cta_ * 8 + 5] = clock64();                                            \
+    }                                                                                    \
   } while (0)
 #else
 #define LAGA_TRACE_DEFINE(name)
 #define LAGA_TRACE_POINT(name, tag, step) \
   do {                                    \
+  } while (0)
+#define LAGA_TRACE_CTA_BEGIN(name) \
+  do {                             \
+  } while (0)
+#define LAGA_TRACE_CTA_END(name) \
+  do {                           \
   } while (0)
 #endif
