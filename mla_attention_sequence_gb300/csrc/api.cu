@@ -178,6 +178,18 @@ CuTensorMapEncodeTiled encode_fn() {
 
 void set_last_error(const char* msg) { std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
 
+int sm_count() {
+  static int counts[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 int* device_status_ptr() {
   static int* ptrs[64] = {};
   static std::mutex mu;

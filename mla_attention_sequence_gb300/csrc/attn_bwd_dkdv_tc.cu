@@ -60,6 +60,7 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return 8u * k + 16u * (k
 struct Params {
   int* status;
   int Sq, S, n_h, q_offset, causal, skv_pad, sq_pad;
+  int successor;  // linear block distance to the CTA that will next run on this SM (the SM count)
   float scale, scale_log2;
   const float* lse2;
   const float* delta;
@@ -71,7 +72,9 @@ struct Params {
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                          const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
-                         const __grid_constant__ CUtensorMap mdO, const Params p) {
+                         const __grid_constant__ CUtensorMap mdO, const __grid_constant__ CUtensorMap mdV,
+                         const __grid_constant__ CUtensorMap mdK, const __grid_constant__ CUtensorMap mdKR,
+                         const Params p) {
   extern __shared__ uint8_t smem_raw[];
   LAGA_TRACE_CTA_BEGIN(dkdv);
   LAGA_TRACE_POINT(dkdv, 30, 0);
@@ -89,7 +92,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* ds_full = bars + 12;
   uint64_t* acc_done = bars + 13;
   uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* epi_full = bars + 15;  // epilogue tiles staged in shared memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(ds_full, SOFTMAX_WARPS);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(epi_full, SOFTMAX_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -140,6 +145,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_load_3d(smem + OFF_K + 2 * KBOX, &mR, kv_full, 0, kv0, b);
       tma_load_2d(smem + OFF_V, &mV, kv_full, h * 128, krow);
       tma_load_2d(smem + OFF_V + KBOX, &mV, kv_full, h * 128 + 64, krow);
+      {
+        // Warm L2 with the first tiles of the CTA that will run next on this SM
+        // (about one CTA lifetime from now): its start then waits on L2, not HBM.
+        const long long nx = gridDim.x, ny = gridDim.y;
+        const long long nb = blockIdx.x + nx * (blockIdx.y + ny * blockIdx.z) + p.successor;
+        if (nb < nx * ny * gridDim.z) {
+          const int nkv0 = static_cast<int>(nb % nx) * BKV;
+          const int nh = static_cast<int>((nb / nx) % ny);
+          const int nbb = static_cast<int>(nb / (nx * ny));
+          const int nrow = nbb * p.skv_pad + nkv0;
+          tma_prefetch_2d(&mK, nh * 128, nrow);
+          tma_prefetch_2d(&mK, nh * 128 + 64, nrow);
+          tma_prefetch_3d(&mR, 0, nkv0, nbb);
+          tma_prefetch_2d(&mV, nh * 128, nrow);
+          tma_prefetch_2d(&mV, nh * 128 + 64, nrow);
+          const int nfirst = p.causal ? max(0, nkv0 - p.q_offset) / BQ : 0;
+          const int nq = (p.Sq + BQ - 1) / BQ;
+          for (int k = nfirst; k < nfirst + 2 && k < nq; ++k) {
+            tma_prefetch_3d(&mQ, nh * 192, k * BQ, nbb);
+            tma_prefetch_3d(&mQ, nh * 192 + 64, k * BQ, nbb);
+            tma_prefetch_3d(&mQ, nh * 192 + 128, k * BQ, nbb);
+            tma_prefetch_3d(&mdO, nh * 128, k * BQ, nbb);
+            tma_prefetch_3d(&mdO, nh * 128 + 64, k * BQ, nbb);
+          }
+        }
+      }
       int i = 0;
       for (; i < n_qt; ++i) {
         const int s = i % NSTAGE;
@@ -175,9 +206,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto stage_desc = [&](int i, uint32_t off, uint32_t lbo) {
       return sdesc_sw128(smem_u32(smem + OFF_STAGE + (i % NSTAGE) * STAGE_BYTES + off), lbo, 1024);
     };
-    auto wait_q = [&](int i) {
-      return warp_wait_or_abort(&q_full[i % NSTAGE], (i / NSTAGE) & 1, abort_flag, 53);
-    };
     auto issue_s = [&](int i) {  // S^T(i) = K Q_i^T
       const uint64_t q_desc = stage_desc(i, 0, 16);
       const uint32_t d = tmem + COL_S + 64u * (i & 1);
@@ -199,59 +227,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       mma_commit_warp(dp_full);
     };
+    // One loop issues everything, the first steps included, so that every MMA
+    // group exists once in the binary: code run once per CTA falls out of the
+    // instruction cache between CTAs and then issues several times slower.
+    // Iteration i: dV(i), dK(i) (i >= 0); dP(i+1) (0 <= i+1 < n); S(i+2) (i+2 < n).
     // Each barrier is tested (without blocking) before the MMA group that precedes
     // its use, so the check after that group costs no shared-memory round trip
     // behind the MMAs.
-    uint32_t tp = 0;
-    if (ok && n_qt > 0) {
-      ok = wait_q(0);
-      if (ok) {
+    uint32_t tp = 0, tq = 0;
+    for (int i = -2; i < n_qt && ok; ++i) {
+      if (i >= 0) {
+        if (!warp_wait_token(&p_full[i & 1], (i >> 1) & 1, tp, abort_flag, 54)) { ok = false; break; }
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 5, i);
+        const uint32_t td = mbar_test(ds_full, i & 1);
         tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-        issued = true;
-        if (n_qt > 1) ok = wait_q(1);
-      }
-      if (ok) {
-        tp = mbar_test(&p_full[0], 0);
-        if (n_qt > 1) {
-          tc_fence_after();
-          issue_s(1);
-        }
-      }
-    }
-    for (int i = 0; i < n_qt && ok; ++i) {
-      if (!warp_wait_token(&p_full[i & 1], (i >> 1) & 1, tp, abort_flag, 54)) { ok = false; break; }
-      const uint32_t td = mbar_test(ds_full, i & 1);
-      tc_fence_after();
-      // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
-      const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
-      const uint32_t pt = tmem + COL_S + 64u * (i & 1);
+        // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
+        const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
+        const uint32_t pt = tmem + COL_S + 64u * (i & 1);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ts_warp(tmem + COL_DV, pt + packed_col(k), do_mn + ((k * 2048) >> 4), IDESC_DV, (i > 0 || k > 0) ? 1u : 0u);
-      if (!warp_wait_token(ds_full, i & 1, td, abort_flag, 55)) { ok = false; break; }
-      const uint32_t tq = i + 2 < n_qt ? mbar_test(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1) : 1u;
-      tc_fence_after();
-      // dK += dS^T Q_i : all 192 head dims in one product
-      const uint64_t q_mn = stage_desc(i, 0, QBOX);
+        for (int k = 0; k < 4; ++k)
+          mma_ts_warp(tmem + COL_DV, pt + packed_col(k), do_mn + ((k * 2048) >> 4), IDESC_DV,
+                      (i > 0 || k > 0) ? 1u : 0u);
+        if (!warp_wait_token(ds_full, i & 1, td, abort_flag, 55)) { ok = false; break; }
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, i);
+        tq = i + 2 < n_qt ? mbar_test(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1) : 1u;
+        tc_fence_after();
+        // dK += dS^T Q_i : all 192 head dims in one product
+        const uint64_t q_mn = stage_desc(i, 0, QBOX);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ts_warp(tmem + COL_DK, tmem + COL_DP + packed_col(k), q_mn + ((k * 2048) >> 4), IDESC_DK,
-                    (i > 0 || k > 0) ? 1u : 0u);
-      mma_commit_warp(&q_empty[i % NSTAGE]);
-      if (i + 1 < n_qt) issue_dp(i + 1);
+        for (int k = 0; k < 4; ++k)
+          mma_ts_warp(tmem + COL_DK, tmem + COL_DP + packed_col(k), q_mn + ((k * 2048) >> 4), IDESC_DK,
+                      (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit_warp(&q_empty[i % NSTAGE]);
+      }
+      if (i + 1 >= 0 && i + 1 < n_qt) issue_dp(i + 1);  // its stage was waited for before S(i+1)
       if (i + 2 < n_qt) {
         if (!warp_wait_token(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, tq, abort_flag, 53)) {
           ok = false;
           break;
         }
-        tp = mbar_test(&p_full[(i + 1) & 1], ((i + 1) >> 1) & 1);
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 7, i + 2);
+        tp = i + 1 >= 0 ? mbar_test(&p_full[(i + 1) & 1], ((i + 1) >> 1) & 1) : 0u;
         tc_fence_after();
         issue_s(i + 2);
+        issued = true;
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 8, i + 2);
       } else {
         tp = 0;  // no group left to hide the test behind: wait in full
       }
+      if (i < 0) tq = 0;
     }
     if (ok) {
       mma_commit_warp(acc_done);
@@ -338,22 +362,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && warp_wait(acc_done, 0, 64)) {
       LAGA_TRACE_POINT(dkdv, 29, 0);
       tc_fence_after();
-      const long long row = static_cast<long long>(b) * p.skv_pad + kv;
-      const long long ncol = static_cast<long long>(p.n_h) * 128;
-      bf16* dv = p.dv_ws + row * ncol + h * 128;
-      bf16* dk = p.dk_ws + row * ncol + h * 128;
-      float* dkr = p.dkr_ws + (row * p.n_h + h) * 64;
+      // Every MMA is done, so the Q/dO stage ring is free: stage the tiles there
+      // in the 128-byte-swizzled box layout and write them with tensor-map stores.
+      // Boxes (16 KB each): 0,1 dV columns [0,64),[64,128); 2,3 dK_nope; 4,5 this
+      // head's RoPE-key gradient (fp32) columns [0,32),[32,64).
       // TMEM columns: dV 0..127, dK 128..319 (no-RoPE 128..255, RoPE 256..319);
-      // warpgroup 0 writes chunks 0..4, warpgroup 1 chunks 5..9 (32 columns each)
+      // warpgroup 0 reads chunks 0..4, warpgroup 1 chunks 5..9 (32 columns each)
+      uint8_t* stg = smem + OFF_STAGE;
 #pragma unroll 1
       for (int c = 5 * half; c < 5 * half + 5; ++c) {
         uint32_t u[32];
         tmem_ld32(tmem + lane_off + c * 32, u);
         tmem_wait_ld();
+        if (n_qt <= 0) {  // no query sees this key tile: the accumulators were never written
+#pragma unroll
+          for (int k = 0; k < 32; ++k) u[k] = 0u;
+        }
         if (c < 8) {
           const float sc = c < 4 ? 1.f : p.scale;
-          bf16* dst = c < 4 ? dv + c * 32 : dk + (c - 4) * 32;
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
+          uint8_t* box = stg + (c >> 1) * 16384;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
@@ -361,15 +388,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * sc, __uint_as_float(u[8 * v + 3]) * sc);
             w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * sc, __uint_as_float(u[8 * v + 5]) * sc);
             w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * sc, __uint_as_float(u[8 * v + 7]) * sc);
-            d4[v] = w;
+            *reinterpret_cast<uint4*>(box + sw128_offset(r, (c & 1) * 4 + v)) = w;
           }
         } else {
-          float4* d4 = reinterpret_cast<float4*>(dkr + (c - 8) * 32);
+          uint8_t* box = stg + (4 + c - 8) * 16384;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            d4[v] = make_float4(__uint_as_float(u[4 * v]) * p.scale, __uint_as_float(u[4 * v + 1]) * p.scale,
-                                __uint_as_float(u[4 * v + 2]) * p.scale, __uint_as_float(u[4 * v + 3]) * p.scale);
+          for (int v = 0; v < 8; ++v) {
+            uint4 w;
+            w.x = __float_as_uint(__uint_as_float(u[4 * v + 0]) * p.scale);
+            w.y = __float_as_uint(__uint_as_float(u[4 * v + 1]) * p.scale);
+            w.z = __float_as_uint(__uint_as_float(u[4 * v + 2]) * p.scale);
+            w.w = __float_as_uint(__uint_as_float(u[4 * v + 3]) * p.scale);
+            *reinterpret_cast<uint4*>(box + sw128_offset(r, v)) = w;
+          }
         }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epi_full);
+      if (warp == 2 && lane == 0 && mbar_wait_or_abort(epi_full, 0, abort_flag, 65)) {
+        const int row = b * p.skv_pad + kv0;
+        tma_store_2d(&mdV, stg, h * 128, row);
+        tma_store_2d(&mdV, stg + 16384, h * 128 + 64, row);
+        tma_store_2d(&mdK, stg + 2 * 16384, h * 128, row);
+        tma_store_2d(&mdK, stg + 3 * 16384, h * 128 + 64, row);
+        tma_store_2d(&mdKR, stg + 4 * 16384, h * 64, row);
+        tma_store_2d(&mdKR, stg + 5 * 16384, h * 64 + 32, row);
+        bulk_commit_group();
+        bulk_wait_all();
       }
     }
   }
@@ -425,6 +471,25 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
     r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  CUtensorMap mdV, mdK, mdKR;  // epilogue stores
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t dims[2] = {kv_inner, kv_rows};
+    const uint64_t strides[1] = {kv_inner * 2};
+    const uint32_t box[2] = {64, BKV};
+    r.cu = make_tmap(&mdV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.dv_ws, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r.cu == CUDA_SUCCESS)
+      r.cu = make_tmap(&mdK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.dk_ws, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 64;
+    const uint64_t dims[2] = {inner, kv_rows};
+    const uint64_t strides[1] = {inner * 4};
+    const uint32_t box[2] = {32, BKV};
+    r.cu = make_tmap(&mdKR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w.dkr_ws, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (r.cu != CUDA_SUCCESS) {
     r.what = "tensor maps attention backward (dK, dV)";
     return r;
@@ -445,12 +510,13 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
   p.dk_ws = w.dk_ws;
   p.dv_ws = w.dv_ws;
   p.dkr_ws = w.dkr_ws;
+  p.successor = sm_count();
   r.err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (r.err != cudaSuccess) {
     r.what = "cudaFuncSetAttribute(attn_bwd_dkdv)";
     return r;
   }
-  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
+  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, mdV, mdK, mdKR, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_bwd_dkdv_kernel launch";
   return r;

@@ -213,43 +213,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_ts_warp(tmem + COL_DQ, ds + packed_col(k), k_mn + ((k * 2048) >> 4), IDESC_DQ, (j > 0 || k > 0) ? 1u : 0u);
       mma_commit_warp(&k_empty[s]);
     };
+    // One loop issues everything, the first step included, so that every MMA group
+    // exists once in the binary: code run once per CTA falls out of the
+    // instruction cache between CTAs and then issues several times slower.
+    // Iteration j: S(j+1), dP(j+1) (j+1 < n), then dq(j) (j >= 0); S and dP of
+    // j+1 go ahead of dq(j) so that the softmax of j+1 overlaps dq(j).
     uint32_t tk = 0;
-    if (ok) {
-      ok = warp_wait_or_abort(&k_full[0], 0, abort_flag, 74);
-      if (ok) {
-        const uint32_t tv = mbar_test(&v_full[0], 0);
-        tc_fence_after();
-        issue_s(0);
-        issued = true;
-        ok = warp_wait_token(&v_full[0], 0, tv, abort_flag, 75);
-      }
-      if (ok) {
-        tk = n_kv > 1 ? mbar_test(&k_full[1 % NSTAGE], (1 / NSTAGE) & 1) : 1u;
-        tc_fence_after();
-        issue_dp(0);
-      }
-    }
-    for (int j = 0; j < n_kv && ok; ++j) {
+    for (int j = -1; j < n_kv && ok; ++j) {
       const uint32_t dph = (j >> 1) & 1;
-      uint32_t td;
-      if (j + 1 < n_kv) {  // S(j+1) and dP(j+1) go ahead of dq(j): softmax of j+1 overlaps dq(j)
+      uint32_t td = 0;
+      if (j + 1 < n_kv) {
         const int jn = j + 1, sn = jn % NSTAGE;
         const uint32_t pn = (jn / NSTAGE) & 1;
         if (!warp_wait_token(&k_full[sn], pn, tk, abort_flag, 74)) { ok = false; break; }
         const uint32_t tv = mbar_test(&v_full[sn], pn);
         tc_fence_after();
         issue_s(jn);
+        issued = true;
         if (!warp_wait_token(&v_full[sn], pn, tv, abort_flag, 75)) { ok = false; break; }
-        td = mbar_test(&ds_full[j & 1], dph);
+        if (j >= 0) td = mbar_test(&ds_full[j & 1], dph);
         tc_fence_after();
         issue_dp(jn);
-      } else {
+      } else if (j >= 0) {
         td = mbar_test(&ds_full[j & 1], dph);
       }
-      if (!warp_wait_token(&ds_full[j & 1], dph, td, abort_flag, 76)) { ok = false; break; }
-      tk = j + 2 < n_kv ? mbar_test(&k_full[(j + 2) % NSTAGE], ((j + 2) / NSTAGE) & 1) : 1u;
-      tc_fence_after();
-      issue_dq(j);
+      if (j >= 0) {
+        if (!warp_wait_token(&ds_full[j & 1], dph, td, abort_flag, 76)) { ok = false; break; }
+        tk = j + 2 < n_kv ? mbar_test(&k_full[(j + 2) % NSTAGE], ((j + 2) / NSTAGE) & 1) : 1u;
+        tc_fence_after();
+        issue_dq(j);
+      } else {
+        tk = n_kv > 1 ? mbar_test(&k_full[1 % NSTAGE], (1 / NSTAGE) & 1) : 1u;
+      }
     }
     if (ok) {
       mma_commit_warp(dq_done);

@@ -43,11 +43,7 @@ constexpr int K_STAGES = 3;
 constexpr int PREFETCH = 4;
 constexpr int V_STAGES = 2;
 constexpr int SMEM_BYTES = K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
-#ifdef LAGA_TRACE
-constexpr int NTHREADS = 288;  // warps 7 and 8 stamp K and V tile arrivals
-#else
 constexpr int NTHREADS = 224;
-#endif
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
 constexpr uint32_t COL_Q = 384;
@@ -175,17 +171,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (j < n_kv)
         for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&v_full[i & 1], (i >> 1) & 1);
     }
-#ifdef LAGA_TRACE
-  } else if (warp == 7 || warp == 8) {
-    if (lane == 0) {
-      for (int j = 0; j < n_kv; ++j) {
-        uint64_t* bar = warp == 7 ? &k_full[j % K_STAGES] : &v_full[j & 1];
-        const uint32_t ph = warp == 7 ? (j / K_STAGES) & 1 : (j >> 1) & 1;
-        if (!mbar_wait_or_abort(bar, ph, abort_flag, 30)) break;
-        LAGA_TRACE_POINT(fwd, warp == 7 ? 22 : 23, j);
-      }
-    }
-#endif
   } else if (warp == 1) {
     // The whole warp runs the issue loop; an elected lane issues. Each barrier is
     // tested (without blocking) before the MMA group that precedes its use, so the
@@ -204,28 +189,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mma_commit_warp(pv_done);
       mma_commit_warp(&v_empty[s]);
     };
+    // One loop issues everything, the last PV included, so that every MMA group
+    // exists once in the binary (code run once per CTA falls out of the
+    // instruction cache between CTAs and then issues several times slower).
+    // Iteration j: S(j) (j < n), then PV(j-1) (j >= 1).
     uint32_t tk = 0, tp = 0, tv = 0;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j & 1;
-      const int ks = j % K_STAGES;
-      if (!warp_wait_token(&k_full[ks], (j / K_STAGES) & 1, tk, abort_flag, 16)) {
-        ok = false;
-        break;
-      }
-      if (j >= 1) {
-        tp = mbar_test(&p_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
-        tv = mbar_test(&v_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
-      }
-      tc_fence_after();
-      const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
-      const uint32_t d_tmem = tmem + s * 128;
+    for (int j = 0; j <= n_kv && ok; ++j) {
+      if (j < n_kv) {
+        const int s = j & 1;
+        const int ks = j % K_STAGES;
+        if (!warp_wait_token(&k_full[ks], (j / K_STAGES) & 1, tk, abort_flag, 16)) {
+          ok = false;
+          break;
+        }
+        if (j >= 1) {
+          tp = mbar_test(&p_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
+          tv = mbar_test(&v_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        }
+        tc_fence_after();
+        const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
+        const uint32_t d_tmem = tmem + s * 128;
 #pragma unroll
-      for (int kk = 0; kk < 12; ++kk)  // head dims [16kk, 16kk + 16): Q columns [8kk, 8kk + 8)
-        mma_ts_warp(d_tmem, tmem + COL_Q + kk * 8, k_desc + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4), IDESC_S,
-                    kk > 0 ? 1u : 0u);
-      issued = true;
-      mma_commit_warp(&s_full[s]);
-      mma_commit_warp(&k_empty[ks]);
+        for (int kk = 0; kk < 12; ++kk)  // head dims [16kk, 16kk + 16): Q columns [8kk, 8kk + 8)
+          mma_ts_warp(d_tmem, tmem + COL_Q + kk * 8, k_desc + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4), IDESC_S,
+                      kk > 0 ? 1u : 0u);
+        issued = true;
+        mma_commit_warp(&s_full[s]);
+        mma_commit_warp(&k_empty[ks]);
+      } else {
+        tp = tv = 0;  // nothing left to hide the tests behind
+      }
       if (j >= 1) {
         const uint32_t ph = ((j - 1) >> 1) & 1;
         if (!warp_wait_token(&p_full[(j - 1) & 1], ph, tp, abort_flag, 14) ||
@@ -238,16 +231,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         issue_pv(j - 1);
       } else {
         tk = 0;
-      }
-    }
-    if (ok) {
-      const int jl = n_kv - 1;
-      const uint32_t ph = (jl >> 1) & 1;
-      ok = warp_wait_or_abort(&p_full[jl & 1], ph, abort_flag, 14) &&
-           warp_wait_or_abort(&v_full[jl & 1], ph, abort_flag, 15);
-      if (ok) {
-        tc_fence_after();
-        issue_pv(jl);
       }
     }
     if (!ok && issued) {
@@ -286,19 +269,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool valid = q_row < p.Sq;
       const uint4* qrow = reinterpret_cast<const uint4*>(
           p.q + ((static_cast<long long>(b) * p.Sq + (valid ? q_row : 0)) * p.n_h + h) * 192);
-#pragma unroll 1
-      for (int c = 0; c < 3; ++c) {
-        uint32_t w[32];
+      uint32_t w[96];  // all 24 loads in flight at once
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = valid ? __ldg(qrow + 8 * c + k) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * k + 0] = v.x;
-          w[4 * k + 1] = v.y;
-          w[4 * k + 2] = v.z;
-          w[4 * k + 3] = v.w;
-        }
-        tmem_st32(tmem + COL_Q + lane_off + 32 * c, w);
+      for (int k = 0; k < 24; ++k) {
+        const uint4 v = valid ? __ldg(qrow + k) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * k + 0] = v.x;
+        w[4 * k + 1] = v.y;
+        w[4 * k + 2] = v.z;
+        w[4 * k + 3] = v.w;
       }
+#pragma unroll
+      for (int c = 0; c < 3; ++c) tmem_st32(tmem + COL_Q + lane_off + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -32,6 +32,8 @@ struct LaunchResult {
 // Device address of this device's status word (timeouts of bounded waits);
 // nullptr if it cannot be resolved.
 int* device_status_ptr();
+// Number of SMs of the current device (cached per device).
+int sm_count();
 
 // Sets the message laga_mla_last_error returns on this host thread.
 void set_last_error(const char* msg);

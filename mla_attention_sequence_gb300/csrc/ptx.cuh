@@ -89,6 +89,17 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
                : "memory");
 }
 
+// Tensor-map store of one box shared -> global (bulk-group completion). Global
+// writes outside the tensor are clipped; x must keep the 16-byte rule.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk store of this thread has completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Plain (non-tensor) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
