@@ -7,24 +7,18 @@
 // against the shared k_rope tile (K = 64), accumulated into one TMEM tile.
 //
 // Warp roles (224 threads):
-//   warp 0      lane 0: TMA for K tiles (3-stage ring)
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
+//   warp 0      lane 0: TMA for Q once, then K tiles
+//   warp 1      TMEM allocation; the whole warp runs the MMA issue loop
 //   warps 2..5  softmax: one query row per thread (TMEM lane), online max and
 //               sum in the log2 domain, P written back over S as bf16 pairs,
 //               O rescaled in TMEM when the running max grows, final epilogue
 //   warp 6      lane 0: TMA for V tiles
-// The two TMA producers sit in different warps: as two lanes of one warp their
-// loops diverge, and a lane blocked waiting for a free slot holds back the other
-// lane's copies.
-// TMEM columns: S/P buffer 0 [0,128), S/P buffer 1 [128,256), O [256,384),
-// Q [384,480). Q is the same for every key tile, so each softmax thread loads
-// its query row from global memory straight into TMEM once and S = Q K^T reads
-// it from there (A operand from TMEM). Q never occupies shared memory, which
-// leaves room for a third K stage: a 48 KB K tile takes longer to arrive under
-// full load than one key-tile step lasts, and two stages left the MMA issuer
-// waiting for K at every step.
-// MMA order S(0), S(1), PV(0), S(2), PV(1), ... lets softmax of tile j+1
-// overlap the PV product of tile j.
+// TMEM columns: three S/P buffers [0,128), [128,256), [256,384); O [384,512).
+// With three buffers the score tile S(j+1) is ready before the softmax of tile
+// j ends: MMA order S(0) S(1) S(2) PV(0) S(3) PV(1) S(4) ..., S(j+3) reusing the
+// buffer that PV(j) has just read. The softmax warps then run back to back and
+// the step costs the larger of the MMA time and the softmax time rather than a
+// chain of both.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -36,17 +30,18 @@ namespace {
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int BOX = 16384;  // one [128 rows][64 cols] bf16 box
+constexpr int Q_BYTES = 3 * BOX;
 constexpr int K_BYTES = 3 * BOX;
 constexpr int V_BYTES = 2 * BOX;
-constexpr int K_STAGES = 3;
+constexpr int K_STAGES = 2;
+constexpr int V_STAGES = 2;
+constexpr int NBUF = 3;  // S/P buffers in TMEM
 // K/V tiles are prefetched into L2 this many tiles ahead of their TMA load.
 constexpr int PREFETCH = 4;
-constexpr int V_STAGES = 2;
-constexpr int SMEM_BYTES = K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
+constexpr int SMEM_BYTES = Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
 constexpr int NTHREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256;
-constexpr uint32_t COL_Q = 384;
+constexpr uint32_t COL_O = 384;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, false, true);
 constexpr float LOG2E = 1.4426950408889634f;
@@ -58,8 +53,7 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 struct FwdParams {
   int* status;  // device status word (timeouts)
   int Sq, S, n_h, q_offset, causal, skv_pad, n_q_tiles;
-  float scale_log2;  // softmax scale * log2(e)
-  const bf16* q;     // [B][Sq][n_h][192]
+  float scale_log2;  // softmax scale * log2(e), > 0
   bf16* out;
   float* lse;
 };
@@ -70,26 +64,28 @@ __device__ __forceinline__ int n_kv_tiles(const FwdParams& p, int t) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mR,
-                    const __grid_constant__ CUtensorMap mV, const FwdParams p) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
+                    const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   LAGA_TRACE_CTA_BEGIN(fwd);
   LAGA_TRACE_POINT(fwd, 30, 0);
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* sK = smem;
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + Q_BYTES;
   uint8_t* sV = sK + K_STAGES * K_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + V_STAGES * V_BYTES);
-  uint64_t* k_full = bars + 0;   // [K_STAGES]
-  uint64_t* k_empty = bars + 3;  // [K_STAGES]
-  uint64_t* v_full = bars + 6;   // [V_STAGES]
-  uint64_t* v_empty = bars + 8;  // [V_STAGES]
-  uint64_t* s_full = bars + 10;  // [2]
-  uint64_t* p_full = bars + 12;  // [2]
-  uint64_t* pv_done = bars + 14;
-  uint64_t* drain = bars + 15;
-  uint64_t* q_tmem = bars + 16;  // Q written into TMEM by the softmax warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;    // [K_STAGES]
+  uint64_t* k_empty = bars + 3;   // [K_STAGES]
+  uint64_t* v_full = bars + 5;    // [V_STAGES]
+  uint64_t* v_empty = bars + 7;   // [V_STAGES]
+  uint64_t* s_full = bars + 9;    // [NBUF]
+  uint64_t* p_full = bars + 12;   // [NBUF]
+  uint64_t* pv_done = bars + 15;  // [NBUF] PV(j) -> pv_done[j % NBUF]
+  uint64_t* drain = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -101,19 +97,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int n_kv = n_kv_tiles(p, t);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < K_STAGES; ++i) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < NBUF; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
     }
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
-    mbar_init(q_tmem, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -128,8 +124,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mR);
+      mbar_arrive_expect_tx(q_full, Q_BYTES);
+      tma_load_3d(sQ, &mQ, q_full, h * 192, t * BQ, b);
+      tma_load_3d(sQ + BOX, &mQ, q_full, h * 192 + 64, t * BQ, b);
+      tma_load_3d(sQ + 2 * BOX, &mQ, q_full, h * 192 + 128, t * BQ, b);
       int j = 0;
       for (; j < n_kv; ++j) {
         const int s = j % K_STAGES;
@@ -146,17 +147,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_prefetch_2d(&mK, h * 128 + 64, row + PREFETCH * BKV);
         }
       }
-      if (j < n_kv)  // aborted: let issued copies land
+      if (j < n_kv) {  // aborted: let issued copies land
+        mbar_drain(q_full, 0);
         for (int i = j - K_STAGES < 0 ? 0 : j - K_STAGES; i < j; ++i)
           mbar_drain(&k_full[i % K_STAGES], (i / K_STAGES) & 1);
+      }
     }
   } else if (warp == 6) {
     if (lane == 0) {
       tma_prefetch_desc(&mV);
       int j = 0;
       for (; j < n_kv; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_or_abort(&v_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, 12)) break;
+        const int s = j % V_STAGES;
+        LAGA_TRACE_POINT(fwd, 24, j);
+        if (!mbar_wait_or_abort(&v_empty[s], ((j / V_STAGES) & 1) ^ 1, abort_flag, 12)) break;
         LAGA_TRACE_POINT(fwd, 21, j);
         uint8_t* dst = sV + s * V_BYTES;
         mbar_arrive_expect_tx(&v_full[s], V_BYTES);
@@ -169,69 +173,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (j < n_kv)
-        for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_drain(&v_full[i & 1], (i >> 1) & 1);
+        for (int i = j - V_STAGES < 0 ? 0 : j - V_STAGES; i < j; ++i)
+          mbar_drain(&v_full[i % V_STAGES], (i / V_STAGES) & 1);
     }
   } else if (warp == 1) {
-    // The whole warp runs the issue loop; an elected lane issues. Each barrier is
-    // tested (without blocking) before the MMA group that precedes its use, so the
-    // check after that group costs no shared-memory round trip behind the MMAs.
-    bool ok = warp_wait_or_abort(q_tmem, 0, abort_flag, 13);
+    // The whole warp runs the issue loop; an elected lane issues. One loop issues
+    // everything (code run once per CTA falls out of the instruction cache between
+    // CTAs and then issues several times slower). Iteration j: PV(j) (j >= 0),
+    // then S(j+3) (j+3 < n). Each barrier is tested (without blocking) before the
+    // MMA group that precedes its use, so the check after that group costs no
+    // shared-memory round trip behind the MMAs.
+    bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 13);
     bool issued = false;
-    tc_fence_after();
-    auto issue_pv = [&](int jj) {
-      const int s = jj & 1;
-      const uint64_t v_desc = sdesc_sw128(smem_u32(sV + s * V_BYTES), BOX, 1024);
-      const uint32_t p_tmem = tmem + s * 128;
-#pragma unroll
-      for (int kk = 0; kk < BKV / 16; ++kk)
-        mma_ts_warp(tmem + COL_O, p_tmem + kk * 8, v_desc + ((kk * 2048) >> 4), IDESC_PV,
-                    (jj > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_warp(pv_done);
-      mma_commit_warp(&v_empty[s]);
-    };
-    // One loop issues everything, the last PV included, so that every MMA group
-    // exists once in the binary (code run once per CTA falls out of the
-    // instruction cache between CTAs and then issues several times slower).
-    // Iteration j: S(j) (j < n), then PV(j-1) (j >= 1).
+    const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     uint32_t tk = 0, tp = 0, tv = 0;
-    for (int j = 0; j <= n_kv && ok; ++j) {
-      if (j < n_kv) {
-        const int s = j & 1;
-        const int ks = j % K_STAGES;
-        if (!warp_wait_token(&k_full[ks], (j / K_STAGES) & 1, tk, abort_flag, 16)) {
+    for (int j = -NBUF; j < n_kv && ok; ++j) {
+      if (j >= 0) {
+        const int vs = j % V_STAGES;
+        if (!warp_wait_token(&p_full[j % NBUF], (j / NBUF) & 1, tp, abort_flag, 14) ||
+            !warp_wait_token(&v_full[vs], (j / V_STAGES) & 1, tv, abort_flag, 15)) {
           ok = false;
           break;
         }
-        if (j >= 1) {
-          tp = mbar_test(&p_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
-          tv = mbar_test(&v_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        if (lane == 0) LAGA_TRACE_POINT(fwd, 3, j);
+        const int jn = j + NBUF;
+        tk = jn < n_kv ? mbar_test(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1) : 1u;
+        tc_fence_after();
+        const uint64_t v_desc = sdesc_sw128(smem_u32(sV + vs * V_BYTES), BOX, 1024);
+        const uint32_t p_tmem = tmem + (j % NBUF) * 128;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          mma_ts_warp(tmem + COL_O, p_tmem + kk * 8, v_desc + ((kk * 2048) >> 4), IDESC_PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_warp(&pv_done[j % NBUF]);
+        mma_commit_warp(&v_empty[vs]);
+        if (lane == 0) LAGA_TRACE_POINT(fwd, 5, j);
+      }
+      const int jn = j + NBUF;
+      if (jn < n_kv) {
+        const int ks = jn % K_STAGES;
+        if (!warp_wait_token(&k_full[ks], (jn / K_STAGES) & 1, tk, abort_flag, 16)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) LAGA_TRACE_POINT(fwd, 1, jn);
+        if (j + 1 >= 0 && j + 1 < n_kv) {
+          tp = mbar_test(&p_full[(j + 1) % NBUF], ((j + 1) / NBUF) & 1);
+          tv = mbar_test(&v_full[(j + 1) % V_STAGES], ((j + 1) / V_STAGES) & 1);
         }
         tc_fence_after();
         const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
-        const uint32_t d_tmem = tmem + s * 128;
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk)  // head dims [16kk, 16kk + 16): Q columns [8kk, 8kk + 8)
-          mma_ts_warp(d_tmem, tmem + COL_Q + kk * 8, k_desc + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4), IDESC_S,
-                      kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 12; ++kk) {  // head dims [16kk, 16kk + 16)
+          const uint32_t off = ((kk >> 2) * BOX + (kk & 3) * 32) >> 4;
+          mma_ss_warp(tmem + (jn % NBUF) * 128, q_desc + off, k_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+        }
         issued = true;
-        mma_commit_warp(&s_full[s]);
+        mma_commit_warp(&s_full[jn % NBUF]);
         mma_commit_warp(&k_empty[ks]);
+        if (lane == 0) LAGA_TRACE_POINT(fwd, 2, jn);
       } else {
         tp = tv = 0;  // nothing left to hide the tests behind
       }
-      if (j >= 1) {
-        const uint32_t ph = ((j - 1) >> 1) & 1;
-        if (!warp_wait_token(&p_full[(j - 1) & 1], ph, tp, abort_flag, 14) ||
-            !warp_wait_token(&v_full[(j - 1) & 1], ph, tv, abort_flag, 15)) {
-          ok = false;
-          break;
-        }
-        tk = j + 1 < n_kv ? mbar_test(&k_full[(j + 1) % K_STAGES], ((j + 1) / K_STAGES) & 1) : 1u;
-        tc_fence_after();
-        issue_pv(j - 1);
-      } else {
-        tk = 0;
-      }
+      if (j < -1) tk = 0;
     }
     if (!ok && issued) {
       mma_commit_warp(drain);
@@ -245,9 +249,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int q_row = t * BQ + r;  // local query index
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int limit = p.causal ? p.q_offset + q_row : p.S - 1;  // last visible key
-    float m_run = -INFINITY;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY;  // running max of the scaled (log2-domain) scores
     float l_run = 0.f;
-    int pv_seen = 0;  // PV completions observed on pv_done
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
       bool w = true;
@@ -256,69 +260,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();  // order lane 0's acquire before the other lanes' reads
       return all;
     };
-    auto wait_pv = [&](int upto) -> bool {  // until PV(upto) has completed
-      while (pv_seen <= upto) {
-        if (!warp_wait(pv_done, pv_seen & 1, 17)) return false;
-        ++pv_seen;
-      }
-      return true;
-    };
-    // Q row r -> TMEM lane r as packed bf16 pairs (the A-operand layout of a
-    // TS-MMA): head dims 2i, 2i+1 become TMEM column i. Rows past Sq are zero.
-    {
-      const bool valid = q_row < p.Sq;
-      const uint4* qrow = reinterpret_cast<const uint4*>(
-          p.q + ((static_cast<long long>(b) * p.Sq + (valid ? q_row : 0)) * p.n_h + h) * 192);
-      uint32_t w[96];  // all 24 loads in flight at once
-#pragma unroll
-      for (int k = 0; k < 24; ++k) {
-        const uint4 v = valid ? __ldg(qrow + k) : make_uint4(0u, 0u, 0u, 0u);
-        w[4 * k + 0] = v.x;
-        w[4 * k + 1] = v.y;
-        w[4 * k + 2] = v.z;
-        w[4 * k + 3] = v.w;
-      }
-#pragma unroll
-      for (int c = 0; c < 3; ++c) tmem_st32(tmem + COL_Q + lane_off + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(w + 32 * c));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_tmem);
-    }
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !wait_pv(j - 2)) {
-        ok = false;
-        break;
-      }
-      if (!warp_wait(&s_full[s], (j >> 1) & 1, 18)) {
+      const int buf = j % NBUF;
+      // S(j) is issued after PV(j-3), so its completion also means P(j-3) in this
+      // buffer has been read.
+      if (!warp_wait(&s_full[buf], (j / NBUF) & 1, 18)) {
         ok = false;
         break;
       }
       if (lane == 0) LAGA_TRACE_POINT(fwd, 10, j);
       tc_fence_after();
-      const uint32_t s_addr = tmem + s * 128 + lane_off;
-      float x[128];
-      {
-        uint32_t u[32];
+      const uint32_t s_addr = tmem + buf * 128 + lane_off;
+      uint32_t x[128];  // raw fp32 scores of this row
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(s_addr + c * 32, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(u[i]) * p.scale_log2;
-        }
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+      tmem_wait_ld();
       const int kv0 = j * BKV;
       if (kv0 + BKV - 1 > limit) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (kv0 + i > limit) x[i] = -INFINITY;
+          if (kv0 + i > limit) x[i] = 0xff800000u;  // -inf
       }
       if (lane == 0) LAGA_TRACE_POINT(fwd, 11, j);
-      float mt = x[0];
+      // max of the raw scores (the scale is positive), four independent chains
+      float m4[4];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
+      for (int a = 0; a < 4; ++a) m4[a] = __uint_as_float(x[a]);
+#pragma unroll
+      for (int i = 4; i < 128; i += 8) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          m4[a] = max3f(m4[a], __uint_as_float(x[i + 2 * a]), __uint_as_float(x[i + 2 * a + 1]));
+      }
+      const float mt = max3f(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sl2;
       float m_use = m_run;
       float alpha = 1.f;
       bool rescale = false;
@@ -330,31 +304,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         rescale = true;
       }
       // rows with nothing visible yet keep p = 0
-      const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      float sum = 0.f;
+      const float neg_m = m_use == -INFINITY ? 0.f : -m_use;
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(x[2 * i] - m_sub);
-        const float p1 = ex2_approx(x[2 * i + 1] - m_sub);
-        sum += p0 + p1;
+        const float p0 = ex2_approx(fmaf(__uint_as_float(x[2 * i]), sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(x[2 * i + 1]), sl2, neg_m));
+        sum2[i & 1] = add_f32x2(sum2[i & 1], make_float2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
-      l_run = l_run * alpha + sum;
+      l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
       m_run = m_use;
       if (lane == 0) LAGA_TRACE_POINT(fwd, 12, j);
-      {
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = pk[c * 32 + i];
-          tmem_st32(s_addr + c * 32, w);
-        }
-      }
+      tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       if (__any_sync(0xffffffffu, rescale)) {
         // O may only be touched once PV(j-1) has landed.
-        if (!wait_pv(j - 1)) {
+        if (j >= 1 && !warp_wait(&pv_done[(j - 1) % NBUF], ((j - 1) / NBUF) & 1, 17)) {
           ok = false;
           break;
         }
@@ -373,10 +340,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[s]);
+      if (lane == 0) mbar_arrive(&p_full[buf]);
       if (lane == 0) LAGA_TRACE_POINT(fwd, 13, j);
     }
-    if (ok && wait_pv(n_kv - 1)) {
+    if (ok && warp_wait(&pv_done[(n_kv - 1) % NBUF], ((n_kv - 1) / NBUF) & 1, 19)) {
       LAGA_TRACE_POINT(fwd, 29, 0);
       tc_fence_after();
       const uint32_t o_addr = tmem + COL_O + lane_off;
@@ -421,15 +388,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace
 
-// The [rows][64] boxes of the operands: 2D maps over the [B*skv_pad][n_h*128]
-// K/V workspace, 3D k_rope map over [B][S][64]. q is read row by row.
+// The [rows][64] boxes of the operands: 3D q map over [B][Sq][n_h*192], 2D maps
+// over the [B*skv_pad][n_h*128] K/V workspace, 3D k_rope map over [B][S][64].
 LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const bf16* v_ws, const bf16* k_rope,
                          bf16* out, float* lse, cudaStream_t st) {
   LaunchResult r;
-  CUtensorMap mK, mR, mV;
+  CUtensorMap mQ, mK, mR, mV;
+  {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 192;
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
+    const uint32_t box[3] = {64, 128, 1};
+    r.cu = make_tmap(&mQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   const uint64_t kv_inner = static_cast<uint64_t>(d.n_h) * 128;
   const uint64_t kv_rows = static_cast<uint64_t>(d.B) * d.skv_pad;
-  {
+  if (r.cu == CUDA_SUCCESS) {
     const uint64_t dims[2] = {kv_inner, kv_rows};
     const uint64_t strides[1] = {kv_inner * 2};
     const uint32_t box[2] = {64, 128};
@@ -457,7 +431,6 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
   p.skv_pad = d.skv_pad;
   p.n_q_tiles = (d.Sq + BQ - 1) / BQ;
   p.scale_log2 = d.scale * LOG2E;
-  p.q = q;
   p.out = out;
   p.lse = lse;
   p.status = device_status_ptr();
@@ -466,7 +439,7 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
     r.what = "cudaFuncSetAttribute(attn_fwd)";
     return r;
   }
-  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mK, mR, mV, p);
+  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_fwd_kernel launch";
   return r;

@@ -159,47 +159,55 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      int it = 0;
-      int local = 0;
-      bool ok = true;
-      bool issued = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
-        const int buf = local & 1;
-        const uint32_t use = static_cast<uint32_t>(local >> 1);
-        if (!mbar_wait_or_abort(&acc_empty[buf], (use & 1) ^ 1, abort_flag, 2)) {
+    // The whole warp runs the issue loop; an elected lane issues. The barrier of
+    // the next k-block (and, before a tile's last k-block, the next accumulator)
+    // is tested without blocking ahead of the current MMAs, so the check after
+    // them costs no shared-memory round trip behind the MMA queue.
+    int it = 0;
+    int local = 0;
+    bool ok = true;
+    bool issued = false;
+    uint32_t tf = 0, ta = 0;
+    const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), C::A_MN ? 8192 : 16, 1024);
+    const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), C::B_MN ? 8192 : 16, 1024);
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!warp_wait_token(&acc_empty[buf], (use & 1) ^ 1, ta, abort_flag, 2)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (!warp_wait_token(&full[s], (it / STAGES) & 1, tf, abort_flag, 3)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait_or_abort(&full[s], ph, abort_flag, 3)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * C::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + s * C::B_BYTES);
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = C::A_MN ? sdesc_sw128(a_base + k * 2048, 8192, 1024)
-                                        : sdesc_sw128(a_base + k * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? sdesc_sw128(b_base + k * 2048, 8192, 1024)
-                                        : sdesc_sw128(b_base + k * 32, 16, 1024);
-            mma_ss(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
-          }
-          issued = true;
-          mma_commit(&empty[s]);
+        tf = mbar_test(&full[(it + 1) % STAGES], ((it + 1) / STAGES) & 1);
+        if (kb == p.k_blocks - 1) {
+          const int nl = local + 1;
+          ta = mbar_test(&acc_empty[nl & 1], ((static_cast<uint32_t>(nl >> 1)) & 1) ^ 1);
         }
-        if (ok) mma_commit(&acc_full[buf]);
+        tc_fence_after();
+        const uint64_t a_stage = a_desc0 + ((s * C::A_BYTES) >> 4);
+        const uint64_t b_stage = b_desc0 + ((s * C::B_BYTES) >> 4);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = a_stage + ((C::A_MN ? k * 2048 : k * 32) >> 4);
+          const uint64_t bd = b_stage + ((C::B_MN ? k * 2048 : k * 32) >> 4);
+          mma_ss_warp(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+        issued = true;
+        mma_commit_warp(&empty[s]);
       }
-      if (!ok && issued) {
-        mma_commit(drain);
-        mbar_drain(drain, 0);
-      }
+      if (ok) mma_commit_warp(&acc_full[buf]);
+    }
+    if (!ok && issued) {
+      mma_commit_warp(drain);
+      if (lane == 0) mbar_drain(drain, 0);
+      __syncwarp();
     }
   } else {
     // Epilogue warps 2..5: warp (w % 4) may read TMEM lanes 32*(w%4) .. +31.
@@ -263,13 +271,6 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
 }
 
 template <int MODE, int BN, int STAGES>
