@@ -308,8 +308,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, 62)) { ok = false; break; }
       if (lane == 0) LAGA_TRACE_POINT(dkdv, 10, i);
       tc_fence_after();
-      const float* lse = reinterpret_cast<const float*>(smem + OFF_ROWV) + s * 2 * BQ + 32 * half;
-      const float* dlt = lse + BQ;
+      // this half-tile's 32 lse and D values (16-byte aligned rows in shared memory)
+      const float4* lse4 = reinterpret_cast<const float4*>(smem + OFF_ROWV) + (s * 2 * BQ + 32 * half) / 4;
+      float lse[32], dlt[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 a = lse4[k], d = lse4[k + BQ / 4];
+        lse[4 * k + 0] = a.x;
+        lse[4 * k + 1] = a.y;
+        lse[4 * k + 2] = a.z;
+        lse[4 * k + 3] = a.w;
+        dlt[4 * k + 0] = d.x;
+        dlt[4 * k + 1] = d.y;
+        dlt[4 * k + 2] = d.z;
+        dlt[4 * k + 3] = d.w;
+      }
       const uint32_t s_addr = tmem + COL_S + 64u * (i & 1) + lane_off;
       float pr[32];
       {
