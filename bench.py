@@ -53,6 +53,35 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# DRAM traffic per launch of a kernel, from one ncu capture of the kernel source
+# identified by `src_sha` (sha256 of the kernel file followed by csrc/ptx.cuh,
+# first 16 hex digits). It is reported only while the source is unchanged.
+# attn_bwd_dkdv: dram__bytes_read.sum + dram__bytes_write.sum = 634.5 + 757.1 MB
+# on the n_h = 64 last-rank shard (the full n_h = 128 shard exceeds the size rule
+# for a --set full capture); the kernel's work and both byte streams (K/V and
+# Q/dO tiles in, dK/dV/dK_rope out) scale with the head count, so x2.
+MEASURED_TRAFFIC = {
+    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "14502f67794b3c99",
+                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (634.515456e6 + 757.129984e6)}},
+}
+
+
+def kernel_traffic(kernel: str, workload: str):
+    import hashlib
+    m = MEASURED_TRAFFIC.get(kernel)
+    if not m or workload not in m["bytes_per_launch"]:
+        return None
+    csrc = os.path.join(ROOT, "mla_attention_sequence_gb300", "csrc")
+    try:
+        h = hashlib.sha256()
+        for name in (m["src"], "ptx.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    return m["bytes_per_launch"][workload] if h.hexdigest()[:16] == m["src_sha"] else None
+
+
 def workload_config(p: Problem, extra=None):
     c = {"workload": p.name, "B": p.B, "Sq": p.Sq, "S": p.S, "n_h": p.n_h, "d_c": p.d_c, "d_nope": p.d_nope,
          "d_rope": p.d_rope, "d_v": p.d_v, "q_offset": p.q_offset, "causal": p.causal, "sp": 8,
@@ -365,7 +394,8 @@ def run_ours(args, name: str):
         achieved = kflops[dom] / (t_step * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak,
+                "traffic": kernel_traffic(dom, problems[0].name) if len(problems) == 1 else None,
                 "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
                 "flops_per_launch": kflops[dom] / len(problems), "ms_per_launch": t_step / len(problems),
                 "launches_per_step": len(problems)}
