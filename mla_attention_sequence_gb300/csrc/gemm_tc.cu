@@ -6,10 +6,11 @@
 //   DCKV       dc_kv = dK_nope W_UK^T + dV W_UV^T          per batch element
 //   DW         dW_UK = sum_b c_kv[b]^T dK_nope[b], dW_UV likewise
 //
-// One persistent kernel template serves all three. Warp roles (192 threads):
-//   warp 0      TMA producer into a STAGES-deep shared-memory ring
-//   warp 1      TMEM allocator and single-thread MMA issuer
+// One persistent kernel template serves all three. Warp roles (224 threads):
+//   warp 0      TMA producer of the A tiles into a STAGES-deep shared-memory ring
+//   warp 1      TMEM allocator; the whole warp runs the MMA issue loop
 //   warps 2..5  epilogue: TMEM -> registers -> bf16 -> global
+//   warp 6      TMA producer of the B tiles
 // Two TMEM accumulators let the epilogue of one tile overlap the next tile's
 // main loop. Operand tiles use the 128-byte swizzle; a K-major tile is
 // [rows][64 K] (128-byte rows), an MN-major tile is a set of [64 K][64 MN] boxes.
@@ -17,6 +18,8 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+
+LAGA_TRACE_DEFINE(gemm)
 
 namespace laga {
 namespace {
@@ -40,6 +43,25 @@ struct GemmParams {
   int rows_valid;              // output rows (per batch element) that exist
 };
 
+// Tile order: within a batch element, bands of GROUP_M m-tiles are walked n by n
+// (m fastest inside a band). The CTAs running at one time then cover a block of
+// about GROUP_M x (SMs / GROUP_M) tiles, so each A and B tile is wanted by a few
+// CTAs at once instead of an m-row of 128 CTAs all asking L2 for the same A tile.
+constexpr int GROUP_M = 8;
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& b, int& m, int& n) {
+  const int tiles_per_batch = p.m_tiles * p.n_tiles;
+  b = tile / tiles_per_batch;
+  const int t = tile - b * tiles_per_batch;
+  const int per_band = GROUP_M * p.n_tiles;
+  const int band = t / per_band;
+  const int first_m = band * GROUP_M;
+  const int gm = min(p.m_tiles - first_m, GROUP_M);
+  const int r = t - band * per_band;
+  m = first_m + r % gm;
+  n = r / gm;
+}
+
 template <int MODE, int BN, int STAGES>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -56,7 +78,7 @@ struct Cfg {
 };
 
 template <int MODE, int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
                    const GemmParams p) {
@@ -80,7 +102,7 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -103,19 +125,25 @@ __global__ void __launch_bounds__(192, 1)
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
   const int num_tiles = tiles_per_batch * p.batches;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      tma_prefetch_desc(&mapA0);
-      tma_prefetch_desc(&mapA1);
-      tma_prefetch_desc(&mapB0);
-      tma_prefetch_desc(&mapB1);
+      // Two producers, in different warps: warp 0 loads the A tiles, warp 6 the B
+      // tiles, each announcing its own bytes on the stage's full barrier (count 2).
+      // One thread issuing both streams tops out well below the fill rate the SM
+      // can take; copies from separate threads proceed side by side.
+      const bool load_a = warp == 0;
+      if (load_a) {
+        tma_prefetch_desc(&mapA0);
+        tma_prefetch_desc(&mapA1);
+      } else {
+        tma_prefetch_desc(&mapB0);
+        tma_prefetch_desc(&mapB1);
+      }
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int b = tile / tiles_per_batch;
-        const int rem = tile - b * tiles_per_batch;
-        const int m = rem / p.n_tiles;
-        const int n = rem - m * p.n_tiles;
+        int b, m, n;
+        tile_coords(p, tile, b, m, n);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -123,32 +151,41 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          if (MODE == RECON_FWD && load_a && it < 512) LAGA_TRACE_POINT(gemm, 20, it);
+          mbar_arrive_expect_tx(&full[s], load_a ? C::A_BYTES : C::B_BYTES);
           uint8_t* a = sA + s * C::A_BYTES;
           uint8_t* bsm = sB + s * C::B_BYTES;
           if constexpr (MODE == RECON_FWD) {
             const bool second = n >= p.n_tiles_first;
             const int n0 = (second ? n - p.n_tiles_first : n) * BN;
-            tma_load_3d(a, &mapA0, &full[s], kb * BK, m * BM, b);
-            const CUtensorMap* mb = second ? &mapB1 : &mapB0;
+            if (load_a) {
+              tma_load_3d(a, &mapA0, &full[s], kb * BK, m * BM, b);
+            } else {
+              const CUtensorMap* mb = second ? &mapB1 : &mapB0;
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(bsm + i * 8192, mb, &full[s], n0 + 64 * i, kb * BK);
+              for (int i = 0; i < BN / 64; ++i) tma_load_2d(bsm + i * 8192, mb, &full[s], n0 + 64 * i, kb * BK);
+            }
           } else if constexpr (MODE == DCKV) {
             const bool second = kb >= p.kb_first;
             const int kk = second ? kb - p.kb_first : kb;
-            tma_load_2d(a, second ? &mapA1 : &mapA0, &full[s], kk * BK, b * p.skv_pad + m * BM);
-            tma_load_2d(bsm, second ? &mapB1 : &mapB0, &full[s], kk * BK, n * BN);
+            if (load_a)
+              tma_load_2d(a, second ? &mapA1 : &mapA0, &full[s], kk * BK, b * p.skv_pad + m * BM);
+            else
+              tma_load_2d(bsm, second ? &mapB1 : &mapB0, &full[s], kk * BK, n * BN);
           } else {
             const bool second = n >= p.n_tiles_first;
             const int n0 = (second ? n - p.n_tiles_first : n) * BN;
             const int bb = kb / p.kb_per_batch;
             const int kk = kb - bb * p.kb_per_batch;
-            tma_load_2d(a, &mapA0, &full[s], m * BM, bb * p.S + kk * BK);
-            tma_load_2d(a + 8192, &mapA0, &full[s], m * BM + 64, bb * p.S + kk * BK);
-            const CUtensorMap* mb = second ? &mapB1 : &mapB0;
+            if (load_a) {
+              tma_load_2d(a, &mapA0, &full[s], m * BM, bb * p.S + kk * BK);
+              tma_load_2d(a + 8192, &mapA0, &full[s], m * BM + 64, bb * p.S + kk * BK);
+            } else {
+              const CUtensorMap* mb = second ? &mapB1 : &mapB0;
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(bsm + i * 8192, mb, &full[s], n0 + 64 * i, bb * p.skv_pad + kk * BK);
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_2d(bsm + i * 8192, mb, &full[s], n0 + 64 * i, bb * p.skv_pad + kk * BK);
+            }
           }
         }
       }
@@ -185,6 +222,7 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
+        if (MODE == RECON_FWD && lane == 0 && it < 512) LAGA_TRACE_POINT(gemm, 1, it);
         tf = mbar_test(&full[(it + 1) % STAGES], ((it + 1) / STAGES) & 1);
         if (kb == p.k_blocks - 1) {
           const int nl = local + 1;
@@ -222,10 +260,8 @@ __global__ void __launch_bounds__(192, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const int b = tile / tiles_per_batch;
-      const int rem = tile - b * tiles_per_batch;
-      const int m = rem / p.n_tiles;
-      const int n = rem - m * p.n_tiles;
+      int b, m, n;
+      tile_coords(p, tile, b, m, n);
       bf16* out;
       int n0;
       if constexpr (MODE == DCKV) {
@@ -261,6 +297,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (MODE == RECON_FWD && lane == 0 && local < 512) LAGA_TRACE_POINT(gemm, 10, local);
     }
   }
 
@@ -289,7 +326,7 @@ LaunchResult launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUt
   const int grid = std::min(tiles, sm_count());
   GemmParams pp = p;
   pp.status = device_status_ptr();
-  kern<<<grid, 192, C::SMEM, st>>>(a0, a1, b0, b1, pp);
+  kern<<<grid, 224, C::SMEM, st>>>(a0, a1, b0, b1, pp);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "gemm_tc_kernel launch";
   return r;
