@@ -387,7 +387,9 @@ LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, con
 
 LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws, const bf16* W_UK,
                              const bf16* W_UV, bf16* dc_kv, cudaStream_t st) {
-  constexpr int BN = 128;
+  // N = 256 halves the operand bytes per MMA cycle against N = 128 (the k-blocks
+  // stream 48 KB per 512 tensor cycles instead of 32 KB per 256).
+  const int BN = d.d_c % 256 == 0 ? 256 : 128;
   LaunchResult r;
   CUtensorMap a0, a1, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;  // reduction length of each pair
@@ -414,7 +416,8 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
   p.ldo = d.d_c;
   p.out_batch_stride = static_cast<long long>(d.S) * d.d_c;
   p.rows_valid = d.S;
-  return launch_gemm<DCKV, BN, 6>(a0, a1, b0, b1, p, st);
+  if (BN == 256) return launch_gemm<DCKV, 256, 4>(a0, a1, b0, b1, p, st);
+  return launch_gemm<DCKV, 128, 6>(a0, a1, b0, b1, p, st);
 }
 
 LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws, const bf16* dv_ws, bf16* dW_UK,
