@@ -52,6 +52,11 @@ constexpr uint32_t IDESC_DV = idesc_bf16(128, 128, false, true);   // dV (A from
 constexpr uint32_t IDESC_DK = idesc_bf16(128, 192, false, true);   // dK (A from TMEM)
 constexpr int NTHREADS = 320;
 constexpr uint32_t SOFTMAX_WARPS = 8;
+// A barrier test hidden inside an MMA group sits this many MMAs before the group's
+// end (about 190 tensor-pipe cycles): it returns once the MMAs ahead of it are
+// dispatched, and the ones behind it keep the pipe busy while the warp branches.
+constexpr int TAIL_N64 = 4;   // S^T, dP^T: 48 cycles each
+constexpr int TAIL_N128 = 3;  // dV: 64 cycles each
 
 // TMEM column of packed bf16 chunk k (16 queries) of a 64-query tile: the two
 // warpgroups pack their halves at columns [0,16) and [32,48).
@@ -206,51 +211,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto stage_desc = [&](int i, uint32_t off, uint32_t lbo) {
       return sdesc_sw128(smem_u32(smem + OFF_STAGE + (i % NSTAGE) * STAGE_BYTES + off), lbo, 1024);
     };
-    auto issue_s = [&](int i) {  // S^T(i) = K Q_i^T
+    // Each group may carry one barrier test (tbar != nullptr) near its end; the
+    // test's result is returned as a token for the wait that follows the group.
+    auto issue_s = [&](int i, uint64_t* tbar, uint32_t tpar) -> uint32_t {  // S^T(i) = K Q_i^T
       const uint64_t q_desc = stage_desc(i, 0, 16);
       const uint32_t d = tmem + COL_S + 64u * (i & 1);
+      uint32_t tok = 0;
 #pragma unroll
       for (int kk = 0; kk < 12; ++kk) {
+        if (kk == 12 - TAIL_N64 && tbar != nullptr) tok = mbar_test(tbar, tpar);
         const uint32_t c = kk >> 2, k = kk & 3;
         mma_ss_warp(d, k_desc + ((c * KBOX + k * 32) >> 4), q_desc + ((c * QBOX + k * 32) >> 4), IDESC_ST,
                     kk > 0 ? 1u : 0u);
       }
       mma_commit_warp(&s_full[i & 1]);
+      return tok;
     };
-    auto issue_dp = [&](int i) {  // dP^T(i) = V dO_i^T
+    auto issue_dp = [&](int i, uint64_t* tbar, uint32_t tpar) -> uint32_t {  // dP^T(i) = V dO_i^T
       const uint64_t do_desc = stage_desc(i, Q_BYTES, 16);
+      uint32_t tok = 0;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
+        if (kk == 8 - TAIL_N64 && tbar != nullptr) tok = mbar_test(tbar, tpar);
         const uint32_t c = kk >> 2, k = kk & 3;
         mma_ss_warp(tmem + COL_DP, v_desc + ((c * KBOX + k * 32) >> 4), do_desc + ((c * QBOX + k * 32) >> 4),
                     IDESC_ST, kk > 0 ? 1u : 0u);
       }
       mma_commit_warp(dp_full);
+      return tok;
     };
     // One loop issues everything, the first steps included, so that every MMA
     // group exists once in the binary: code run once per CTA falls out of the
     // instruction cache between CTAs and then issues several times slower.
     // Iteration i: dV(i), dK(i) (i >= 0); dP(i+1) (0 <= i+1 < n); S(i+2) (i+2 < n).
-    // Each barrier is tested (without blocking) before the MMA group that precedes
+    // Each barrier is tested (without blocking) inside the MMA group that precedes
     // its use, so the check after that group costs no shared-memory round trip
-    // behind the MMAs.
+    // behind the MMAs: ds_full inside dV, q_full inside dP, p_full inside S.
     uint32_t tp = 0, tq = 0;
     for (int i = -2; i < n_qt && ok; ++i) {
       if (i >= 0) {
         if (!warp_wait_token(&p_full[i & 1], (i >> 1) & 1, tp, abort_flag, 54)) { ok = false; break; }
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 5, i);
-        const uint32_t td = mbar_test(ds_full, i & 1);
         tc_fence_after();
         // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
         const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
         const uint32_t pt = tmem + COL_S + 64u * (i & 1);
+        uint32_t td = 0;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
+          if (k == 4 - TAIL_N128) td = mbar_test(ds_full, i & 1);
           mma_ts_warp(tmem + COL_DV, pt + packed_col(k), do_mn + ((k * 2048) >> 4), IDESC_DV,
                       (i > 0 || k > 0) ? 1u : 0u);
+        }
         if (!warp_wait_token(ds_full, i & 1, td, abort_flag, 55)) { ok = false; break; }
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, i);
-        tq = i + 2 < n_qt ? mbar_test(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1) : 1u;
         tc_fence_after();
         // dK += dS^T Q_i : all 192 head dims in one product
         const uint64_t q_mn = stage_desc(i, 0, QBOX);
@@ -260,22 +274,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       (i > 0 || k > 0) ? 1u : 0u);
         mma_commit_warp(&q_empty[i % NSTAGE]);
       }
-      if (i + 1 >= 0 && i + 1 < n_qt) issue_dp(i + 1);  // its stage was waited for before S(i+1)
+      if (i + 1 >= 0 && i + 1 < n_qt) {  // its stage was waited for before S(i+1)
+        const bool more = i + 2 < n_qt;
+        tq = issue_dp(i + 1, more ? &q_full[(i + 2) % NSTAGE] : nullptr, ((i + 2) / NSTAGE) & 1);
+      } else {
+        tq = 0;
+      }
       if (i + 2 < n_qt) {
         if (!warp_wait_token(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, tq, abort_flag, 53)) {
           ok = false;
           break;
         }
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 7, i + 2);
-        tp = i + 1 >= 0 ? mbar_test(&p_full[(i + 1) & 1], ((i + 1) >> 1) & 1) : 0u;
         tc_fence_after();
-        issue_s(i + 2);
+        const bool next = i + 1 >= 0;
+        tp = issue_s(i + 2, next ? &p_full[(i + 1) & 1] : nullptr, ((i + 1) >> 1) & 1);
         issued = true;
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 8, i + 2);
       } else {
         tp = 0;  // no group left to hide the test behind: wait in full
       }
-      if (i < 0) tq = 0;
     }
     if (ok) {
       mma_commit_warp(acc_done);

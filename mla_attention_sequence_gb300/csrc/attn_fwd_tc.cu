@@ -49,6 +49,10 @@ constexpr float LOG2E = 1.4426950408889634f;
 // than this many powers of two; exact, since numerator and denominator share
 // the stale max.
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// Barrier tests hidden inside an MMA group sit before its last TEST_TAIL MMAs:
+// the test returns once the MMAs ahead of it are dispatched, and the MMAs behind
+// it keep the tensor pipe busy while the warp branches on the result.
+constexpr int TEST_TAIL = 3;
 
 struct FwdParams {
   int* status;  // device status word (timeouts)
@@ -180,14 +184,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // The whole warp runs the issue loop; an elected lane issues. One loop issues
     // everything (code run once per CTA falls out of the instruction cache between
     // CTAs and then issues several times slower). Iteration j: PV(j) (j >= 0),
-    // then S(j+3) (j+3 < n). Each barrier is tested (without blocking) before the
-    // MMA group that precedes its use, so the check after that group costs no
-    // shared-memory round trip behind the MMAs.
+    // then S(j+3) (j+3 < n). Each barrier is tested (without blocking) inside the
+    // MMA group that precedes its use, TEST_TAIL MMAs before that group's end, so
+    // the check after the group costs no shared-memory round trip behind the MMAs.
     bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 13);
     bool issued = false;
     const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     uint32_t tk = 0, tp = 0, tv = 0;
     for (int j = -NBUF; j < n_kv && ok; ++j) {
+      const int jn = j + NBUF;
       if (j >= 0) {
         const int vs = j % V_STAGES;
         if (!warp_wait_token(&p_full[j % NBUF], (j / NBUF) & 1, tp, abort_flag, 14) ||
@@ -196,20 +201,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         if (lane == 0) LAGA_TRACE_POINT(fwd, 3, j);
-        const int jn = j + NBUF;
-        tk = jn < n_kv ? mbar_test(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1) : 1u;
         tc_fence_after();
         const uint64_t v_desc = sdesc_sw128(smem_u32(sV + vs * V_BYTES), BOX, 1024);
         const uint32_t p_tmem = tmem + (j % NBUF) * 128;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          if (kk == BKV / 16 - TEST_TAIL)
+            tk = jn < n_kv ? mbar_test(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1) : 1u;
           mma_ts_warp(tmem + COL_O, p_tmem + kk * 8, v_desc + ((kk * 2048) >> 4), IDESC_PV,
                       (j > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit_warp(&pv_done[j % NBUF]);
         mma_commit_warp(&v_empty[vs]);
         if (lane == 0) LAGA_TRACE_POINT(fwd, 5, j);
       }
-      const int jn = j + NBUF;
       if (jn < n_kv) {
         const int ks = jn % K_STAGES;
         if (!warp_wait_token(&k_full[ks], (jn / K_STAGES) & 1, tk, abort_flag, 16)) {
@@ -217,14 +222,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         if (lane == 0) LAGA_TRACE_POINT(fwd, 1, jn);
-        if (j + 1 >= 0 && j + 1 < n_kv) {
-          tp = mbar_test(&p_full[(j + 1) % NBUF], ((j + 1) / NBUF) & 1);
-          tv = mbar_test(&v_full[(j + 1) % V_STAGES], ((j + 1) / V_STAGES) & 1);
-        }
         tc_fence_after();
+        const bool next_pv = j + 1 >= 0 && j + 1 < n_kv;
         const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk) {  // head dims [16kk, 16kk + 16)
+          if (kk == 12 - TEST_TAIL && next_pv) {
+            tp = mbar_test(&p_full[(j + 1) % NBUF], ((j + 1) / NBUF) & 1);
+            tv = mbar_test(&v_full[(j + 1) % V_STAGES], ((j + 1) / V_STAGES) & 1);
+          }
           const uint32_t off = ((kk >> 2) * BOX + (kk & 3) * 32) >> 4;
           mma_ss_warp(tmem + (jn % NBUF) * 128, q_desc + off, k_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
