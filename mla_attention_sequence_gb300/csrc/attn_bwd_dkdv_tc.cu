@@ -52,11 +52,10 @@ constexpr uint32_t IDESC_DV = idesc_bf16(128, 128, false, true);   // dV (A from
 constexpr uint32_t IDESC_DK = idesc_bf16(128, 192, false, true);   // dK (A from TMEM)
 constexpr int NTHREADS = 320;
 constexpr uint32_t SOFTMAX_WARPS = 8;
-// A barrier test hidden inside an MMA group sits this many MMAs before the group's
-// end (about 190 tensor-pipe cycles): it returns once the MMAs ahead of it are
-// dispatched, and the ones behind it keep the pipe busy while the warp branches.
-constexpr int TAIL_N64 = 4;   // S^T, dP^T: 48 cycles each
-constexpr int TAIL_N128 = 3;  // dV: 64 cycles each
+// MMAs are issued in blocks (one elect.sync each). A barrier test hidden inside an
+// MMA group sits before the group's last block: it returns once the MMAs ahead of
+// it are dispatched, and the block behind it keeps the pipe busy while the warp
+// branches on the result.
 
 // TMEM column of packed bf16 chunk k (16 queries) of a 64-query tile: the two
 // warpgroups pack their halves at columns [0,16) and [32,48).
@@ -218,11 +217,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t d = tmem + COL_S + 64u * (i & 1);
       uint32_t tok = 0;
 #pragma unroll
-      for (int kk = 0; kk < 12; ++kk) {
-        if (kk == 12 - TAIL_N64 && tbar != nullptr) tok = mbar_test(tbar, tpar);
-        const uint32_t c = kk >> 2, k = kk & 3;
-        mma_ss_warp(d, k_desc + ((c * KBOX + k * 32) >> 4), q_desc + ((c * QBOX + k * 32) >> 4), IDESC_ST,
-                    kk > 0 ? 1u : 0u);
+      for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c
+        if (c == 2 && tbar != nullptr) tok = mbar_test(tbar, tpar);
+        const uint64_t a = k_desc + ((c * KBOX) >> 4), q = q_desc + ((c * QBOX) >> 4);
+        mma4_ss_warp(d, a, a + 2, a + 4, a + 6, q, q + 2, q + 4, q + 6, IDESC_ST, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(&s_full[i & 1]);
       return tok;
@@ -231,11 +229,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t do_desc = stage_desc(i, Q_BYTES, 16);
       uint32_t tok = 0;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        if (kk == 8 - TAIL_N64 && tbar != nullptr) tok = mbar_test(tbar, tpar);
-        const uint32_t c = kk >> 2, k = kk & 3;
-        mma_ss_warp(tmem + COL_DP, v_desc + ((c * KBOX + k * 32) >> 4), do_desc + ((c * QBOX + k * 32) >> 4),
-                    IDESC_ST, kk > 0 ? 1u : 0u);
+      for (int c = 0; c < 2; ++c) {  // value dims [64c, 64c + 64)
+        if (c == 1 && tbar != nullptr) tok = mbar_test(tbar, tpar);
+        const uint64_t a = v_desc + ((c * KBOX) >> 4), o = do_desc + ((c * QBOX) >> 4);
+        mma4_ss_warp(tmem + COL_DP, a, a + 2, a + 4, a + 6, o, o + 2, o + 4, o + 6, IDESC_ST, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(dp_full);
       return tok;
@@ -256,22 +253,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
         const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
         const uint32_t pt = tmem + COL_S + 64u * (i & 1);
-        uint32_t td = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (k == 4 - TAIL_N128) td = mbar_test(ds_full, i & 1);
-          mma_ts_warp(tmem + COL_DV, pt + packed_col(k), do_mn + ((k * 2048) >> 4), IDESC_DV,
-                      (i > 0 || k > 0) ? 1u : 0u);
-        }
+        // two blocks of two (queries [0,32), [32,64)), the ds_full test between them
+        mma2_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), do_mn, do_mn + (2048 >> 4), IDESC_DV,
+                     i > 0 ? 1u : 0u);
+        const uint32_t td = mbar_test(ds_full, i & 1);
+        mma2_ts_warp(tmem + COL_DV, pt + packed_col(2), pt + packed_col(3), do_mn + (4096 >> 4),
+                     do_mn + (6144 >> 4), IDESC_DV, 1u);
         if (!warp_wait_token(ds_full, i & 1, td, abort_flag, 55)) { ok = false; break; }
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, i);
         tc_fence_after();
         // dK += dS^T Q_i : all 192 head dims in one product
         const uint64_t q_mn = stage_desc(i, 0, QBOX);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts_warp(tmem + COL_DK, tmem + COL_DP + packed_col(k), q_mn + ((k * 2048) >> 4), IDESC_DK,
-                      (i > 0 || k > 0) ? 1u : 0u);
+        const uint32_t ds = tmem + COL_DP;
+        mma4_ts_warp(tmem + COL_DK, ds + packed_col(0), ds + packed_col(1), ds + packed_col(2), ds + packed_col(3),
+                     q_mn, q_mn + (2048 >> 4), q_mn + (4096 >> 4), q_mn + (6144 >> 4), IDESC_DK, i > 0 ? 1u : 0u);
         mma_commit_warp(&q_empty[i % NSTAGE]);
       }
       if (i + 1 >= 0 && i + 1 < n_qt) {  // its stage was waited for before S(i+1)

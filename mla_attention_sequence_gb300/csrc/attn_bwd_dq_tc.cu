@@ -192,9 +192,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto issue_s = [&](int j) {  // S(j) = Q K_j^T
       const uint64_t k_desc = sdesc_sw128(smem_u32(smem + OFF_K + (j % K_STAGES) * K_BYTES), 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 12; ++kk) {
-        const uint32_t off = ((kk >> 2) * BOX + (kk & 3) * 32) >> 4;
-        mma_ss_warp(tmem + COL_S, q_desc + off, k_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+      for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c (one elect each)
+        const uint32_t o = (c * BOX) >> 4;
+        mma4_ss_warp(tmem + COL_S, q_desc + o, q_desc + o + 2, q_desc + o + 4, q_desc + o + 6, k_desc + o,
+                     k_desc + o + 2, k_desc + o + 4, k_desc + o + 6, IDESC_S, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(s_full);
     };
@@ -202,9 +203,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int s = j % V_STAGES;
       const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V + s * V_BYTES), 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // head dims [16kk, 16kk + 16): dO columns [8kk, 8kk + 8)
-        mma_ts_warp(tmem + COL_DP, tmem + COL_DO + kk * 8, v_desc + (((kk >> 2) * BOX + (kk & 3) * 32) >> 4),
-                    IDESC_S, kk > 0 ? 1u : 0u);
+      for (int c = 0; c < 2; ++c) {  // head dims [64c, 64c + 64): dO columns [32c, 32c + 32)
+        const uint32_t a = tmem + COL_DO + 32 * c;
+        const uint64_t v = v_desc + ((c * BOX) >> 4);
+        mma4_ts_warp(tmem + COL_DP, a, a + 8, a + 16, a + 24, v, v + 2, v + 4, v + 6, IDESC_S, c > 0 ? 1u : 0u);
+      }
       mma_commit_warp(dp_full);
       mma_commit_warp(&v_empty[s]);
     };
@@ -227,10 +230,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         const int s = j % K_STAGES;
         const uint64_t k_mn = sdesc_sw128(smem_u32(smem + OFF_K + s * K_BYTES), BOX, 1024);
+        const uint32_t ds = tmem + COL_DP;
 #pragma unroll
-        for (int k = 0; k < BKV / 16; ++k)
-          mma_ts_warp(tmem + COL_DQ, tmem + COL_DP + packed_col(k), k_mn + ((k * 2048) >> 4), IDESC_DQ,
-                      (j > 0 || k > 0) ? 1u : 0u);
+        for (int g = 0; g < BKV / 64; ++g) {  // keys [64g, 64g + 64)
+          const int k = 4 * g;
+          mma4_ts_warp(tmem + COL_DQ, ds + packed_col(k), ds + packed_col(k + 1), ds + packed_col(k + 2),
+                       ds + packed_col(k + 3), k_mn + ((k * 2048) >> 4), k_mn + (((k + 1) * 2048) >> 4),
+                       k_mn + (((k + 2) * 2048) >> 4), k_mn + (((k + 3) * 2048) >> 4), IDESC_DQ,
+                       (j > 0 || g > 0) ? 1u : 0u);
+        }
         mma_commit_warp(&k_empty[s]);
       }
       if (jn < n_kv) {  // dP(j+1): follows dq(j), which reads dS(j) from the same columns

@@ -49,10 +49,10 @@ constexpr float LOG2E = 1.4426950408889634f;
 // than this many powers of two; exact, since numerator and denominator share
 // the stale max.
 constexpr float RESCALE_THRESHOLD = 8.0f;
-// Barrier tests hidden inside an MMA group sit before its last TEST_TAIL MMAs:
-// the test returns once the MMAs ahead of it are dispatched, and the MMAs behind
-// it keep the tensor pipe busy while the warp branches on the result.
-constexpr int TEST_TAIL = 3;
+// MMAs are issued in blocks of four (one elect.sync each). A barrier test hidden
+// inside an MMA group sits before the group's last block: it returns once the MMAs
+// ahead of it are dispatched, and the block behind it keeps the tensor pipe busy
+// while the warp branches on the result.
 
 struct FwdParams {
   int* status;  // device status word (timeouts)
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // everything (code run once per CTA falls out of the instruction cache between
     // CTAs and then issues several times slower). Iteration j: PV(j) (j >= 0),
     // then S(j+3) (j+3 < n). Each barrier is tested (without blocking) inside the
-    // MMA group that precedes its use, TEST_TAIL MMAs before that group's end, so
+    // MMA group that precedes its use, before that group's last block of four, so
     // the check after the group costs no shared-memory round trip behind the MMAs.
     bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 13);
     bool issued = false;
@@ -205,11 +205,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint64_t v_desc = sdesc_sw128(smem_u32(sV + vs * V_BYTES), BOX, 1024);
         const uint32_t p_tmem = tmem + (j % NBUF) * 128;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          if (kk == BKV / 16 - TEST_TAIL)
-            tk = jn < n_kv ? mbar_test(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1) : 1u;
-          mma_ts_warp(tmem + COL_O, p_tmem + kk * 8, v_desc + ((kk * 2048) >> 4), IDESC_PV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+        for (int g = 0; g < BKV / 64; ++g) {  // keys [64g, 64g + 64): four K16 steps
+          if (g == BKV / 64 - 1) tk = jn < n_kv ? mbar_test(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1) : 1u;
+          const int kk = 4 * g;
+          mma4_ts_warp(tmem + COL_O, p_tmem + kk * 8, p_tmem + kk * 8 + 8, p_tmem + kk * 8 + 16, p_tmem + kk * 8 + 24,
+                       v_desc + ((kk * 2048) >> 4), v_desc + (((kk + 1) * 2048) >> 4),
+                       v_desc + (((kk + 2) * 2048) >> 4), v_desc + (((kk + 3) * 2048) >> 4), IDESC_PV,
+                       (j > 0 || g > 0) ? 1u : 0u);
         }
         mma_commit_warp(&pv_done[j % NBUF]);
         mma_commit_warp(&v_empty[vs]);
@@ -226,13 +228,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool next_pv = j + 1 >= 0 && j + 1 < n_kv;
         const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {  // head dims [16kk, 16kk + 16)
-          if (kk == 12 - TEST_TAIL && next_pv) {
+        for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c
+          if (c == 2 && next_pv) {
             tp = mbar_test(&p_full[(j + 1) % NBUF], ((j + 1) / NBUF) & 1);
             tv = mbar_test(&v_full[(j + 1) % V_STAGES], ((j + 1) / V_STAGES) & 1);
           }
-          const uint32_t off = ((kk >> 2) * BOX + (kk & 3) * 32) >> 4;
-          mma_ss_warp(tmem + (jn % NBUF) * 128, q_desc + off, k_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+          const uint32_t o = (c * BOX) >> 4;
+          mma4_ss_warp(tmem + (jn % NBUF) * 128, q_desc + o, q_desc + o + 2, q_desc + o + 4, q_desc + o + 6,
+                       k_desc + o, k_desc + o + 2, k_desc + o + 4, k_desc + o + 6, IDESC_S, c > 0 ? 1u : 0u);
         }
         issued = true;
         mma_commit_warp(&s_full[jn % NBUF]);

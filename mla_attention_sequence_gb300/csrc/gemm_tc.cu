@@ -231,12 +231,11 @@ __global__ void __launch_bounds__(224, 1)
         tc_fence_after();
         const uint64_t a_stage = a_desc0 + ((s * C::A_BYTES) >> 4);
         const uint64_t b_stage = b_desc0 + ((s * C::B_BYTES) >> 4);
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = a_stage + ((C::A_MN ? k * 2048 : k * 32) >> 4);
-          const uint64_t bd = b_stage + ((C::B_MN ? k * 2048 : k * 32) >> 4);
-          mma_ss_warp(d_tmem, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
-        }
+        // the k-block's four K16 steps, one elect.sync for the block
+        constexpr uint32_t DA = (C::A_MN ? 2048 : 32) >> 4, DB = (C::B_MN ? 2048 : 32) >> 4;
+        static_assert(BK == 64, "one block of four K16 steps per k-block");
+        mma4_ss_warp(d_tmem, a_stage, a_stage + DA, a_stage + 2 * DA, a_stage + 3 * DA, b_stage, b_stage + DB,
+                     b_stage + 2 * DB, b_stage + 3 * DB, C::IDESC, kb != 0 ? 1u : 0u);
         issued = true;
         mma_commit_warp(&empty[s]);
       }
