@@ -137,10 +137,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // Issue order: what the first MMAs need (the key/value tile, then the first
+      // query stages), and only then the successor's L2 prefetches. Each TMA
+      // instruction takes the issuing thread a while, and S(0) waits on all of
+      // the ones ahead of its tiles.
       tma_prefetch_desc(&mQ);
-      tma_prefetch_desc(&mK);
-      tma_prefetch_desc(&mR);
-      tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mdO);
       mbar_arrive_expect_tx(kv_full, K_BYTES + V_BYTES);
       const int krow = b * p.skv_pad + kv0;
@@ -149,9 +150,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_load_3d(smem + OFF_K + 2 * KBOX, &mR, kv_full, 0, kv0, b);
       tma_load_2d(smem + OFF_V, &mV, kv_full, h * 128, krow);
       tma_load_2d(smem + OFF_V + KBOX, &mV, kv_full, h * 128 + 64, krow);
-      {
-        // Warm L2 with the first tiles of the CTA that will run next on this SM
-        // (about one CTA lifetime from now): its start then waits on L2, not HBM.
+      // Warm L2 with the first tiles of the CTA that will run next on this SM
+      // (about one CTA lifetime from now): its start then waits on L2, not HBM.
+      auto prefetch_successor = [&]() {
         const long long nx = gridDim.x, ny = gridDim.y;
         const long long nb = blockIdx.x + nx * (blockIdx.y + ny * blockIdx.z) + p.successor;
         if (nb < nx * ny * gridDim.z) {
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tma_prefetch_3d(&mdO, nh * 128 + 64, k * BQ, nbb);
           }
         }
-      }
+      };
       int i = 0;
       for (; i < n_qt; ++i) {
         const int s = i % NSTAGE;
@@ -192,7 +193,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const long long roff = (static_cast<long long>(b) * p.n_h + h) * p.sq_pad + q0;
         bulk_load(rows, p.lse2 + roff, ROWV_BYTES, &q_full[s]);
         bulk_load(rows + BQ, p.delta + roff, ROWV_BYTES, &q_full[s]);
+        if (i == NSTAGE - 1 || (i == n_qt - 1 && n_qt < NSTAGE)) prefetch_successor();
       }
+      if (n_qt <= 0) prefetch_successor();
       if (i < n_qt) {
         mbar_drain(kv_full, 0);
         for (int k = i - NSTAGE < 0 ? 0 : i - NSTAGE; k < i; ++k)
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_store_2d(&mdKR, stg + 4 * 16384, h * 64, row);
         tma_store_2d(&mdKR, stg + 5 * 16384, h * 64 + 32, row);
         bulk_commit_group();
-        bulk_wait_all();
+        bulk_wait_read_all();  // the staging memory is read out; the writes finish on their own
       }
     }
   }

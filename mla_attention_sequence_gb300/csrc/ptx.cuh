@@ -99,6 +99,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has completed (writes done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits only until every committed bulk store of this thread has finished reading
+// its shared-memory source: enough before that memory is reused or the CTA exits
+// (the global writes still land before the grid completes).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Plain (non-tensor) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
