@@ -12,9 +12,16 @@
 // touch shared memory. dK covers all 192 head dims in one N = 192 product: the
 // first 128 columns are dK_nope, the last 64 this head's RoPE-key gradient.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warp 0      lane 0: TMA for the key/value tile, then Q, dO, lse, D tiles
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
+//   warp 1      TMEM allocation; issues every tcgen05.mma and touches no shared
+//               memory in its loop: it learns that an operand is ready from
+//   warp 10     the waiter, which waits on each mbarrier the next MMA group needs
+//               and meets warp 1 at a named barrier (the AND of their flags
+//               carries a timeout). Measured on GB300: an mbarrier test in the
+//               MMA warp costs the tensor pipe 150-400 cycles per step once
+//               compute warps share its SM sub-partition; the named barrier
+//               costs it next to nothing.
 //   warps 2..9  two warpgroups; each thread owns one key row (TMEM lane) and
 //               half of the 64 query columns: P^T, dS^T, and half the epilogue
 // TMEM columns: dV [0,128), dK [128,320), S^T/P^T x2 [320,448), dP^T/dS^T [448,512).
@@ -50,12 +57,10 @@ constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 320, COL_DP = 448;
 constexpr uint32_t IDESC_ST = idesc_bf16(128, 64, false, false);   // S^T, dP^T
 constexpr uint32_t IDESC_DV = idesc_bf16(128, 128, false, true);   // dV (A from TMEM)
 constexpr uint32_t IDESC_DK = idesc_bf16(128, 192, false, true);   // dK (A from TMEM)
-constexpr int NTHREADS = 320;
+constexpr int NTHREADS = 352;
+constexpr int WAITER_WARP = 10;
+constexpr int HANDOFF_BAR = 1;  // named barrier of warp 1 and the waiter (64 threads)
 constexpr uint32_t SOFTMAX_WARPS = 8;
-// MMAs are issued in blocks (one elect.sync each). A barrier test hidden inside an
-// MMA group sits before the group's last block: it returns once the MMAs ahead of
-// it are dispatched, and the block behind it keeps the pipe busy while the warp
-// branches on the result.
 
 // TMEM column of packed bf16 chunk k (16 queries) of a 64-query tile: the two
 // warpgroups pack their halves at columns [0,16) and [32,48).
@@ -202,69 +207,90 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mbar_drain(&q_full[k % NSTAGE], (k / NSTAGE) & 1);
       }
     }
+  } else if (warp == WAITER_WARP) {
+    // The waiter walks the MMA warp's waits in the same order: kv_full, then per
+    // step i p_full(i), ds_full(i) (i >= 0) and q_full(i+2) (i + 2 < n). Each wait
+    // ends at the named barrier; a failed wait (timeout or abort) is ANDed in, and
+    // both warps leave their loops at the same hand-off.
+    auto handoff = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+      const bool w = warp_wait_or_abort(bar, parity, abort_flag, where);
+      return bar_and(HANDOFF_BAR, 64, w);
+    };
+    if (handoff(kv_full, 0, 52)) {
+      for (int i = -2; i < n_qt; ++i) {
+        if (i >= 0) {
+          if (!handoff(&p_full[i & 1], (i >> 1) & 1, 54)) break;
+          if (!handoff(ds_full, i & 1, 55)) break;
+        }
+        if (i + 2 < n_qt && !handoff(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, 53)) break;
+      }
+    }
   } else if (warp == 1) {
-    // The whole warp runs the issue loop (warp-uniform waits, elected lane issues).
-    bool ok = warp_wait_or_abort(kv_full, 0, abort_flag, 52);
+    // The whole warp runs the issue loop (an elected lane issues each block of MMAs).
+    // Readiness comes from the waiter through the named barrier, never from a
+    // shared-memory access of this warp.
+    auto ready = [&]() -> bool {
+      const bool r = bar_and(HANDOFF_BAR, 64, true);
+      tc_fence_after();
+      return r;
+    };
+    bool ok = ready();  // key/value tile
     bool issued = false;
-    tc_fence_after();
     const uint64_t k_desc = sdesc_sw128(smem_u32(smem + OFF_K), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
     // K-major (16) and MN-major (QBOX) descriptors of a stage's Q and dO tiles
     auto stage_desc = [&](int i, uint32_t off, uint32_t lbo) {
       return sdesc_sw128(smem_u32(smem + OFF_STAGE + (i % NSTAGE) * STAGE_BYTES + off), lbo, 1024);
     };
-    // Each group may carry one barrier test (tbar != nullptr) near its end; the
-    // test's result is returned as a token for the wait that follows the group.
-    auto issue_s = [&](int i, uint64_t* tbar, uint32_t tpar) -> uint32_t {  // S^T(i) = K Q_i^T
+    auto issue_s = [&](int i) {  // S^T(i) = K Q_i^T
       const uint64_t q_desc = stage_desc(i, 0, 16);
       const uint32_t d = tmem + COL_S + 64u * (i & 1);
-      uint32_t tok = 0;
 #pragma unroll
       for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c
-        if (c == 2 && tbar != nullptr) tok = mbar_test(tbar, tpar);
         const uint64_t a = k_desc + ((c * KBOX) >> 4), q = q_desc + ((c * QBOX) >> 4);
         mma4_ss_warp(d, a, a + 2, a + 4, a + 6, q, q + 2, q + 4, q + 6, IDESC_ST, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(&s_full[i & 1]);
-      return tok;
     };
-    auto issue_dp = [&](int i, uint64_t* tbar, uint32_t tpar) -> uint32_t {  // dP^T(i) = V dO_i^T
+    auto issue_dp = [&](int i) {  // dP^T(i) = V dO_i^T
       const uint64_t do_desc = stage_desc(i, Q_BYTES, 16);
-      uint32_t tok = 0;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // value dims [64c, 64c + 64)
-        if (c == 1 && tbar != nullptr) tok = mbar_test(tbar, tpar);
         const uint64_t a = v_desc + ((c * KBOX) >> 4), o = do_desc + ((c * QBOX) >> 4);
         mma4_ss_warp(tmem + COL_DP, a, a + 2, a + 4, a + 6, o, o + 2, o + 4, o + 6, IDESC_ST, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(dp_full);
-      return tok;
     };
     // One loop issues everything, the first steps included, so that every MMA
     // group exists once in the binary: code run once per CTA falls out of the
     // instruction cache between CTAs and then issues several times slower.
     // Iteration i: dV(i), dK(i) (i >= 0); dP(i+1) (0 <= i+1 < n); S(i+2) (i+2 < n).
-    // Each barrier is tested (without blocking) inside the MMA group that precedes
-    // its use, so the check after that group costs no shared-memory round trip
-    // behind the MMAs: ds_full inside dV, q_full inside dP, p_full inside S.
-    uint32_t tp = 0, tq = 0;
+#ifdef LAGA_TRACE
+    // trace build only: cycles spent at each hand-off
+    long long st_cyc[3] = {0, 0, 0};
+    const long long st_t0 = clock64();
+#define DKDV_STAT_BEGIN(k) const long long w0_##k = clock64();
+#define DKDV_STAT_END(k) st_cyc[k] += clock64() - w0_##k;
+#else
+#define DKDV_STAT_BEGIN(k)
+#define DKDV_STAT_END(k)
+#endif
     for (int i = -2; i < n_qt && ok; ++i) {
       if (i >= 0) {
-        if (!warp_wait_token(&p_full[i & 1], (i >> 1) & 1, tp, abort_flag, 54)) { ok = false; break; }
+        DKDV_STAT_BEGIN(0)
+        if (!ready()) { ok = false; break; }  // P^T(i)
+        DKDV_STAT_END(0)
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 5, i);
-        tc_fence_after();
         // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
         const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
         const uint32_t pt = tmem + COL_S + 64u * (i & 1);
-        // two blocks of two (queries [0,32), [32,64)), the ds_full test between them
-        mma2_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), do_mn, do_mn + (2048 >> 4), IDESC_DV,
+        mma4_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), pt + packed_col(2), pt + packed_col(3),
+                     do_mn, do_mn + (2048 >> 4), do_mn + (4096 >> 4), do_mn + (6144 >> 4), IDESC_DV,
                      i > 0 ? 1u : 0u);
-        const uint32_t td = mbar_test(ds_full, i & 1);
-        mma2_ts_warp(tmem + COL_DV, pt + packed_col(2), pt + packed_col(3), do_mn + (4096 >> 4),
-                     do_mn + (6144 >> 4), IDESC_DV, 1u);
-        if (!warp_wait_token(ds_full, i & 1, td, abort_flag, 55)) { ok = false; break; }
+        DKDV_STAT_BEGIN(1)
+        if (!ready()) { ok = false; break; }  // dS^T(i)
+        DKDV_STAT_END(1)
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, i);
-        tc_fence_after();
         // dK += dS^T Q_i : all 192 head dims in one product
         const uint64_t q_mn = stage_desc(i, 0, QBOX);
         const uint32_t ds = tmem + COL_DP;
@@ -272,27 +298,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      q_mn, q_mn + (2048 >> 4), q_mn + (4096 >> 4), q_mn + (6144 >> 4), IDESC_DK, i > 0 ? 1u : 0u);
         mma_commit_warp(&q_empty[i % NSTAGE]);
       }
-      if (i + 1 >= 0 && i + 1 < n_qt) {  // its stage was waited for before S(i+1)
-        const bool more = i + 2 < n_qt;
-        tq = issue_dp(i + 1, more ? &q_full[(i + 2) % NSTAGE] : nullptr, ((i + 2) / NSTAGE) & 1);
-      } else {
-        tq = 0;
-      }
+      if (i + 1 >= 0 && i + 1 < n_qt) issue_dp(i + 1);  // its stage was handed over before S(i+1)
       if (i + 2 < n_qt) {
-        if (!warp_wait_token(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, tq, abort_flag, 53)) {
-          ok = false;
-          break;
-        }
+        DKDV_STAT_BEGIN(2)
+        if (!ready()) { ok = false; break; }  // Q_{i+2}, dO_{i+2}, lse and D rows
+        DKDV_STAT_END(2)
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 7, i + 2);
-        tc_fence_after();
-        const bool next = i + 1 >= 0;
-        tp = issue_s(i + 2, next ? &p_full[(i + 1) & 1] : nullptr, ((i + 1) >> 1) & 1);
+        issue_s(i + 2);
         issued = true;
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 8, i + 2);
-      } else {
-        tp = 0;  // no group left to hide the test behind: wait in full
       }
     }
+#ifdef LAGA_TRACE
+    if (lane == 0) {
+      for (int k = 0; k < 3; ++k) {
+        LAGA_TRACE_STAT(dkdv, k, 0);
+        LAGA_TRACE_STAT(dkdv, 3 + k, st_cyc[k]);
+      }
+      LAGA_TRACE_STAT(dkdv, 6, clock64() - st_t0);
+      LAGA_TRACE_STAT(dkdv, 7, n_qt);
+    }
+#endif
+#undef DKDV_STAT_BEGIN
+#undef DKDV_STAT_END
     if (ok) {
       mma_commit_warp(acc_done);
     } else if (issued) {

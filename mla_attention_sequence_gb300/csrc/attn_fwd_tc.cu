@@ -81,15 +81,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* sV = sK + K_STAGES * K_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + V_STAGES * V_BYTES);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [K_STAGES]
-  uint64_t* k_empty = bars + 3;   // [K_STAGES]
-  uint64_t* v_full = bars + 5;    // [V_STAGES]
-  uint64_t* v_empty = bars + 7;   // [V_STAGES]
-  uint64_t* s_full = bars + 9;    // [NBUF]
-  uint64_t* p_full = bars + 12;   // [NBUF]
-  uint64_t* pv_done = bars + 15;  // [NBUF] PV(j) -> pv_done[j % NBUF]
-  uint64_t* drain = bars + 18;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* k_full = q_full + 1;          // [K_STAGES]
+  uint64_t* k_empty = k_full + K_STAGES;  // [K_STAGES]
+  uint64_t* v_full = k_empty + K_STAGES;  // [V_STAGES]
+  uint64_t* v_empty = v_full + V_STAGES;  // [V_STAGES]
+  uint64_t* s_full = v_empty + V_STAGES;  // [NBUF]
+  uint64_t* p_full = s_full + NBUF;       // [NBUF]
+  uint64_t* pv_done = p_full + NBUF;      // [NBUF] PV(j) -> pv_done[j % NBUF]
+  uint64_t* drain = pv_done + NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  static_assert((2 + 2 * K_STAGES + 2 * V_STAGES + 3 * NBUF) * 8 + 8 <= 256, "barrier area");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -102,9 +103,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < K_STAGES; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < V_STAGES; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
@@ -191,15 +194,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool issued = false;
     const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
     uint32_t tk = 0, tp = 0, tv = 0;
+#ifdef LAGA_TRACE
+    // trace build only: per wait site, how often the token was unset and the cycles spent
+    long long st_cyc[3] = {0, 0, 0}, st_miss[3] = {0, 0, 0};
+    const long long st_t0 = clock64();
+#endif
     for (int j = -NBUF; j < n_kv && ok; ++j) {
       const int jn = j + NBUF;
       if (j >= 0) {
         const int vs = j % V_STAGES;
+#ifdef LAGA_TRACE
+        const long long w0 = clock64();
+        st_miss[0] += tp ? 0 : 1;
+        st_miss[1] += tv ? 0 : 1;
+#endif
         if (!warp_wait_token(&p_full[j % NBUF], (j / NBUF) & 1, tp, abort_flag, 14) ||
             !warp_wait_token(&v_full[vs], (j / V_STAGES) & 1, tv, abort_flag, 15)) {
           ok = false;
           break;
         }
+#ifdef LAGA_TRACE
+        st_cyc[0] += clock64() - w0;
+#endif
         if (lane == 0) LAGA_TRACE_POINT(fwd, 3, j);
         tc_fence_after();
         const uint64_t v_desc = sdesc_sw128(smem_u32(sV + vs * V_BYTES), BOX, 1024);
@@ -219,10 +235,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (jn < n_kv) {
         const int ks = jn % K_STAGES;
+#ifdef LAGA_TRACE
+        const long long w1 = clock64();
+        st_miss[2] += tk ? 0 : 1;
+#endif
         if (!warp_wait_token(&k_full[ks], (jn / K_STAGES) & 1, tk, abort_flag, 16)) {
           ok = false;
           break;
         }
+#ifdef LAGA_TRACE
+        st_cyc[2] += clock64() - w1;
+#endif
         if (lane == 0) LAGA_TRACE_POINT(fwd, 1, jn);
         tc_fence_after();
         const bool next_pv = j + 1 >= 0 && j + 1 < n_kv;
@@ -246,6 +269,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (j < -1) tk = 0;
     }
+#ifdef LAGA_TRACE
+    if (lane == 0) {
+      for (int k = 0; k < 3; ++k) {
+        LAGA_TRACE_STAT(fwd, k, st_miss[k]);
+        LAGA_TRACE_STAT(fwd, 3 + k, st_cyc[k]);
+      }
+      LAGA_TRACE_STAT(fwd, 6, clock64() - st_t0);
+      LAGA_TRACE_STAT(fwd, 7, n_kv);
+    }
+#endif
     if (!ok && issued) {
       mma_commit_warp(drain);
       if (lane == 0) mbar_drain(drain, 0);

@@ -417,6 +417,21 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
   return all;
 }
 
+// Named barrier `id` over `nthreads` threads (a multiple of 32): every participant
+// contributes `pred` and receives the AND of all contributions.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // Non-blocking test of an mbarrier phase (acquire on success). Meant to be issued
 // by the MMA warp BEFORE a group of tcgen05.mma: a shared-memory access issued
 // right after such a group waits behind it for well over 100 cycles, and a branch
@@ -468,6 +483,12 @@ __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* sta
 #define LAGA_TRACE_DEFINE(name)                                                          \
   __device__ long long g_trace_##name[LAGA_TRACE_CAP];                                  \
   __device__ long long g_cta_##name[LAGA_TRACE_CTAS * 8];                               \
+  __device__ long long g_stat_##name[LAGA_TRACE_CTAS * 8];                              \
+  extern "C" int laga_debug_stat_##name(long long* host, int max) {                      \
+    const int n = max < LAGA_TRACE_CTAS * 8 ? max : LAGA_TRACE_CTAS * 8;                 \
+    cudaMemcpyFromSymbol(host, g_stat_##name, n * sizeof(long long));                   \
+    return n;                                                                            \
+  }                                                                                      \
   extern "C" int laga_debug_trace_##name(long long* host, int max) {                     \
     const int n = max < LAGA_TRACE_CAP ? max : LAGA_TRACE_CAP;                           \
     cudaMemcpyFromSymbol(host, g_trace_##name, n * sizeof(long long));                  \
@@ -507,8 +528,17 @@ __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* sta
       g_cta_##name[cta_ * 8 + 5] = clock64();                                            \
     }                                                                                    \
   } while (0)
+// Per-CTA counters (8 slots) kept in registers by one warp and written once.
+#define LAGA_TRACE_STAT(name, slot, value)                                               \
+  do {                                                                                   \
+    const long long cta_ = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z); \
+    if (cta_ < LAGA_TRACE_CTAS) g_stat_##name[cta_ * 8 + (slot)] = (value);              \
+  } while (0)
 #else
 #define LAGA_TRACE_DEFINE(name)
+#define LAGA_TRACE_STAT(name, slot, value) \
+  do {                                     \
+  } while (0)
 #define LAGA_TRACE_POINT(name, tag, step) \
   do {                                    \
   } while (0)
