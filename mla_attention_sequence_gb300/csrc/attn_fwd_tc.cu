@@ -6,9 +6,14 @@
 // S = Q K^T is the sum of the no-RoPE product (K = 128) and the RoPE product
 // against the shared k_rope tile (K = 64), accumulated into one TMEM tile.
 //
-// Warp roles (224 threads):
+// Warp roles (256 threads):
 //   warp 0      lane 0: TMA for Q once, then K tiles
-//   warp 1      TMEM allocation; the whole warp runs the MMA issue loop
+//   warp 1      TMEM allocation; the whole warp runs the MMA issue loop and
+//               touches no shared memory in it: it learns that an operand is
+//               ready from warp 7 through a named barrier
+//   warp 7      the waiter: waits on each mbarrier the next MMA group needs, then
+//               meets warp 1 at the named barrier (the AND of their flags
+//               carries a timeout)
 //   warps 2..5  softmax: one query row per thread (TMEM lane), online max and
 //               sum in the log2 domain, P written back over S as bf16 pairs,
 //               O rescaled in TMEM when the running max grows, final epilogue
@@ -39,7 +44,9 @@ constexpr int NBUF = 3;  // S/P buffers in TMEM
 // K/V tiles are prefetched into L2 this many tiles ahead of their TMA load.
 constexpr int PREFETCH = 4;
 constexpr int SMEM_BYTES = Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
-constexpr int NTHREADS = 224;
+constexpr int NTHREADS = 256;
+constexpr int WAITER_WARP = 7;
+constexpr int HANDOFF_BAR = 1;  // named barrier of warp 1 and the waiter (64 threads)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 384;
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
@@ -49,10 +56,6 @@ constexpr float LOG2E = 1.4426950408889634f;
 // than this many powers of two; exact, since numerator and denominator share
 // the stale max.
 constexpr float RESCALE_THRESHOLD = 8.0f;
-// MMAs are issued in blocks of four (one elect.sync each). A barrier test hidden
-// inside an MMA group sits before the group's last block: it returns once the MMAs
-// ahead of it are dispatched, and the block behind it keeps the tensor pipe busy
-// while the warp branches on the result.
 
 struct FwdParams {
   int* status;  // device status word (timeouts)
@@ -183,20 +186,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = j - V_STAGES < 0 ? 0 : j - V_STAGES; i < j; ++i)
           mbar_drain(&v_full[i % V_STAGES], (i / V_STAGES) & 1);
     }
+  } else if (warp == WAITER_WARP) {
+    // The waiter walks the MMA warp's waits in the same order: q_full, then per
+    // iteration j p_full(j) and v_full(j) (j >= 0, one hand-off) and k_full(j+3)
+    // (j + 3 < n). A failed wait (timeout or abort) is ANDed in at the named
+    // barrier, and both warps leave their loops at the same hand-off.
+    if (bar_and(HANDOFF_BAR, 64, warp_wait_or_abort(q_full, 0, abort_flag, 13))) {
+      for (int j = -NBUF; j < n_kv; ++j) {
+        const int jn = j + NBUF;
+        if (j >= 0) {
+          const bool w = warp_wait_or_abort(&p_full[j % NBUF], (j / NBUF) & 1, abort_flag, 14) &&
+                         warp_wait_or_abort(&v_full[j % V_STAGES], (j / V_STAGES) & 1, abort_flag, 15);
+          if (!bar_and(HANDOFF_BAR, 64, w)) break;
+        }
+        if (jn < n_kv &&
+            !bar_and(HANDOFF_BAR, 64, warp_wait_or_abort(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1, abort_flag, 16)))
+          break;
+      }
+    }
   } else if (warp == 1) {
-    // The whole warp runs the issue loop; an elected lane issues. One loop issues
-    // everything (code run once per CTA falls out of the instruction cache between
-    // CTAs and then issues several times slower). Iteration j: PV(j) (j >= 0),
-    // then S(j+3) (j+3 < n). Each barrier is tested (without blocking) inside the
-    // MMA group that precedes its use, before that group's last block of four, so
-    // the check after the group costs no shared-memory round trip behind the MMAs.
-    bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 13);
+    // The whole warp runs the issue loop; an elected lane issues each block of
+    // four MMAs. One loop issues everything (code run once per CTA falls out of the
+    // instruction cache between CTAs and then issues several times slower).
+    // Iteration j: PV(j) (j >= 0), then S(j+3) (j+3 < n). Readiness of every
+    // operand comes from the waiter through the named barrier.
+    auto ready = [&]() -> bool {
+      const bool r = bar_and(HANDOFF_BAR, 64, true);
+      tc_fence_after();
+      return r;
+    };
+    bool ok = ready();  // Q
     bool issued = false;
     const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
-    uint32_t tk = 0, tp = 0, tv = 0;
 #ifdef LAGA_TRACE
-    // trace build only: per wait site, how often the token was unset and the cycles spent
-    long long st_cyc[3] = {0, 0, 0}, st_miss[3] = {0, 0, 0};
+    // trace build only: cycles spent at each hand-off
+    long long st_cyc[3] = {0, 0, 0};
     const long long st_t0 = clock64();
 #endif
     for (int j = -NBUF; j < n_kv && ok; ++j) {
@@ -205,11 +229,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int vs = j % V_STAGES;
 #ifdef LAGA_TRACE
         const long long w0 = clock64();
-        st_miss[0] += tp ? 0 : 1;
-        st_miss[1] += tv ? 0 : 1;
 #endif
-        if (!warp_wait_token(&p_full[j % NBUF], (j / NBUF) & 1, tp, abort_flag, 14) ||
-            !warp_wait_token(&v_full[vs], (j / V_STAGES) & 1, tv, abort_flag, 15)) {
+        if (!ready()) {  // P(j) and V(j)
           ok = false;
           break;
         }
@@ -217,12 +238,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         st_cyc[0] += clock64() - w0;
 #endif
         if (lane == 0) LAGA_TRACE_POINT(fwd, 3, j);
-        tc_fence_after();
         const uint64_t v_desc = sdesc_sw128(smem_u32(sV + vs * V_BYTES), BOX, 1024);
         const uint32_t p_tmem = tmem + (j % NBUF) * 128;
 #pragma unroll
         for (int g = 0; g < BKV / 64; ++g) {  // keys [64g, 64g + 64): four K16 steps
-          if (g == BKV / 64 - 1) tk = jn < n_kv ? mbar_test(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1) : 1u;
           const int kk = 4 * g;
           mma4_ts_warp(tmem + COL_O, p_tmem + kk * 8, p_tmem + kk * 8 + 8, p_tmem + kk * 8 + 16, p_tmem + kk * 8 + 24,
                        v_desc + ((kk * 2048) >> 4), v_desc + (((kk + 1) * 2048) >> 4),
@@ -237,9 +256,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ks = jn % K_STAGES;
 #ifdef LAGA_TRACE
         const long long w1 = clock64();
-        st_miss[2] += tk ? 0 : 1;
 #endif
-        if (!warp_wait_token(&k_full[ks], (jn / K_STAGES) & 1, tk, abort_flag, 16)) {
+        if (!ready()) {  // K(j+3)
           ok = false;
           break;
         }
@@ -247,15 +265,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         st_cyc[2] += clock64() - w1;
 #endif
         if (lane == 0) LAGA_TRACE_POINT(fwd, 1, jn);
-        tc_fence_after();
-        const bool next_pv = j + 1 >= 0 && j + 1 < n_kv;
         const uint64_t k_desc = sdesc_sw128(smem_u32(sK + ks * K_BYTES), 16, 1024);
 #pragma unroll
         for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c
-          if (c == 2 && next_pv) {
-            tp = mbar_test(&p_full[(j + 1) % NBUF], ((j + 1) / NBUF) & 1);
-            tv = mbar_test(&v_full[(j + 1) % V_STAGES], ((j + 1) / V_STAGES) & 1);
-          }
           const uint32_t o = (c * BOX) >> 4;
           mma4_ss_warp(tmem + (jn % NBUF) * 128, q_desc + o, q_desc + o + 2, q_desc + o + 4, q_desc + o + 6,
                        k_desc + o, k_desc + o + 2, k_desc + o + 4, k_desc + o + 6, IDESC_S, c > 0 ? 1u : 0u);
@@ -264,15 +276,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_commit_warp(&s_full[jn % NBUF]);
         mma_commit_warp(&k_empty[ks]);
         if (lane == 0) LAGA_TRACE_POINT(fwd, 2, jn);
-      } else {
-        tp = tv = 0;  // nothing left to hide the tests behind
       }
-      if (j < -1) tk = 0;
     }
 #ifdef LAGA_TRACE
     if (lane == 0) {
       for (int k = 0; k < 3; ++k) {
-        LAGA_TRACE_STAT(fwd, k, st_miss[k]);
+        LAGA_TRACE_STAT(fwd, k, 0);
         LAGA_TRACE_STAT(fwd, 3 + k, st_cyc[k]);
       }
       LAGA_TRACE_STAT(fwd, 6, clock64() - st_t0);
