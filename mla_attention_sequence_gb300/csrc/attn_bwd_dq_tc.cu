@@ -184,26 +184,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // everything (code run once per CTA falls out of the instruction cache between
     // CTAs and then issues several times slower). Iteration j: S(j+1) once S(j)
     // is released, dq(j) once dS(j) is in, then dP(j+1). Each barrier is tested
-    // (without blocking) before the MMA group that precedes its use.
+    // (without blocking) inside the MMA group that precedes its use, before that
+    // group's last block of four, and consumed as a token after the group.
     bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 73) && warp_wait_or_abort(do_tmem, 0, abort_flag, 77);
     bool issued = false;
     tc_fence_after();
     const uint64_t q_desc = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
-    auto issue_s = [&](int j) {  // S(j) = Q K_j^T
+    // `tests` runs before the group's last block
+    auto issue_s = [&](int j, auto&& tests) {  // S(j) = Q K_j^T
       const uint64_t k_desc = sdesc_sw128(smem_u32(smem + OFF_K + (j % K_STAGES) * K_BYTES), 16, 1024);
 #pragma unroll
       for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c (one elect each)
+        if (c == 2) tests();
         const uint32_t o = (c * BOX) >> 4;
         mma4_ss_warp(tmem + COL_S, q_desc + o, q_desc + o + 2, q_desc + o + 4, q_desc + o + 6, k_desc + o,
                      k_desc + o + 2, k_desc + o + 4, k_desc + o + 6, IDESC_S, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(s_full);
     };
-    auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T
+    auto issue_dp = [&](int j, auto&& tests) {  // dP(j) = dO V_j^T
       const int s = j % V_STAGES;
       const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V + s * V_BYTES), 16, 1024);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // head dims [64c, 64c + 64): dO columns [32c, 32c + 32)
+        if (c == 1) tests();
         const uint32_t a = tmem + COL_DO + 32 * c;
         const uint64_t v = v_desc + ((c * BOX) >> 4);
         mma4_ts_warp(tmem + COL_DP, a, a + 8, a + 16, a + 24, v, v + 2, v + 4, v + 6, IDESC_S, c > 0 ? 1u : 0u);
@@ -217,22 +221,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (jn < n_kv) {  // S(j+1): needs K(j+1) and S(j) released
         if (j >= 0 && !warp_wait_token(s_free, j & 1, tf, abort_flag, 78)) { ok = false; break; }
         if (!warp_wait_token(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1, tk, abort_flag, 74)) { ok = false; break; }
-        if (j >= 0) td = mbar_test(ds_full, j & 1);
         tc_fence_after();
-        issue_s(jn);
+        issue_s(jn, [&]() {
+          if (j >= 0) td = mbar_test(ds_full, j & 1);
+        });
         issued = true;
       } else if (j >= 0) {
         td = mbar_test(ds_full, j & 1);
       }
       if (j >= 0) {  // dq(j) += dS(j) K_j : A = dS (TMEM, packed bf16), B = key tile MN-major (N = 192)
         if (!warp_wait_token(ds_full, j & 1, td, abort_flag, 76)) { ok = false; break; }
-        if (jn < n_kv) tv = mbar_test(&v_full[jn % V_STAGES], (jn / V_STAGES) & 1);
         tc_fence_after();
         const int s = j % K_STAGES;
         const uint64_t k_mn = sdesc_sw128(smem_u32(smem + OFF_K + s * K_BYTES), BOX, 1024);
         const uint32_t ds = tmem + COL_DP;
 #pragma unroll
         for (int g = 0; g < BKV / 64; ++g) {  // keys [64g, 64g + 64)
+          if (g == BKV / 64 - 1 && jn < n_kv) tv = mbar_test(&v_full[jn % V_STAGES], (jn / V_STAGES) & 1);
           const int k = 4 * g;
           mma4_ts_warp(tmem + COL_DQ, ds + packed_col(k), ds + packed_col(k + 1), ds + packed_col(k + 2),
                        ds + packed_col(k + 3), k_mn + ((k * 2048) >> 4), k_mn + (((k + 1) * 2048) >> 4),
@@ -243,12 +248,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (jn < n_kv) {  // dP(j+1): follows dq(j), which reads dS(j) from the same columns
         if (!warp_wait_token(&v_full[jn % V_STAGES], (jn / V_STAGES) & 1, tv, abort_flag, 75)) { ok = false; break; }
-        if (jn + 1 < n_kv) {
-          tf = mbar_test(s_free, jn & 1);
-          tk = mbar_test(&k_full[(jn + 1) % K_STAGES], ((jn + 1) / K_STAGES) & 1);
-        }
         tc_fence_after();
-        issue_dp(jn);
+        issue_dp(jn, [&]() {
+          if (jn + 1 < n_kv) {
+            tf = mbar_test(s_free, jn & 1);
+            tk = mbar_test(&k_full[(jn + 1) % K_STAGES], ((jn + 1) / K_STAGES) & 1);
+          }
+        });
       }
     }
     if (ok) {
