@@ -197,9 +197,10 @@ __global__ void __launch_bounds__(224, 1)
     }
   } else if (warp == 1) {
     // The whole warp runs the issue loop; an elected lane issues. The barrier of
-    // the next k-block (and, before a tile's last k-block, the next accumulator)
-    // is tested without blocking ahead of the current MMAs, so the check after
-    // them costs no shared-memory round trip behind the MMA queue.
+    // the next k-block (and, in a tile's last k-block, the next accumulator) is
+    // tested without blocking between the current k-block's two pairs of MMAs,
+    // so the check after them costs no shared-memory round trip behind the MMA
+    // queue.
     int it = 0;
     int local = 0;
     bool ok = true;
@@ -223,19 +224,19 @@ __global__ void __launch_bounds__(224, 1)
           break;
         }
         if (MODE == RECON_FWD && lane == 0 && it < 512) LAGA_TRACE_POINT(gemm, 1, it);
+        tc_fence_after();
+        const uint64_t a_stage = a_desc0 + ((s * C::A_BYTES) >> 4);
+        const uint64_t b_stage = b_desc0 + ((s * C::B_BYTES) >> 4);
+        // the k-block's four K16 steps as two pairs, the next barriers tested between them
+        constexpr uint32_t DA = (C::A_MN ? 2048 : 32) >> 4, DB = (C::B_MN ? 2048 : 32) >> 4;
+        static_assert(BK == 64, "four K16 steps per k-block");
+        mma2_ss_warp(d_tmem, a_stage, a_stage + DA, b_stage, b_stage + DB, C::IDESC, kb != 0 ? 1u : 0u);
         tf = mbar_test(&full[(it + 1) % STAGES], ((it + 1) / STAGES) & 1);
         if (kb == p.k_blocks - 1) {
           const int nl = local + 1;
           ta = mbar_test(&acc_empty[nl & 1], ((static_cast<uint32_t>(nl >> 1)) & 1) ^ 1);
         }
-        tc_fence_after();
-        const uint64_t a_stage = a_desc0 + ((s * C::A_BYTES) >> 4);
-        const uint64_t b_stage = b_desc0 + ((s * C::B_BYTES) >> 4);
-        // the k-block's four K16 steps, one elect.sync for the block
-        constexpr uint32_t DA = (C::A_MN ? 2048 : 32) >> 4, DB = (C::B_MN ? 2048 : 32) >> 4;
-        static_assert(BK == 64, "one block of four K16 steps per k-block");
-        mma4_ss_warp(d_tmem, a_stage, a_stage + DA, a_stage + 2 * DA, a_stage + 3 * DA, b_stage, b_stage + DB,
-                     b_stage + 2 * DB, b_stage + 3 * DB, C::IDESC, kb != 0 ? 1u : 0u);
+        mma2_ss_warp(d_tmem, a_stage + 2 * DA, a_stage + 3 * DA, b_stage + 2 * DB, b_stage + 3 * DB, C::IDESC, 1u);
         issued = true;
         mma_commit_warp(&empty[s]);
       }
