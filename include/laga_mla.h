@@ -205,6 +205,15 @@ laga_status laga_mla_profile_enable(int enable);
  * exceed `max`), or -1 if an event query fails. */
 int laga_mla_profile_read(const char** names, float* ms, int max);
 
+/* Failure-path self test. Enqueues on `stream` one CTA whose thread waits on an
+ * mbarrier that nothing ever arrives at, through the same bounded wait every
+ * library kernel uses (2 s, wait site 99). The wait expires, the kernel records
+ * LAGA_ERR_TIMEOUT in this device's status word exactly as a library kernel that
+ * gave up on a wait does, and returns; the CUDA context stays usable. The next
+ * laga_mla_check on the stream then returns LAGA_ERR_TIMEOUT (and clears the
+ * word). Returns LAGA_ERR_CUDA if the launch fails, else LAGA_OK. */
+laga_status laga_mla_selftest_timeout(laga_stream_t stream);
+
 /* Library ABI version: major*10000 + minor*100 + patch. */
 int laga_mla_version(void);
 

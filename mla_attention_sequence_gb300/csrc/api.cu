@@ -213,6 +213,23 @@ CUresult make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// One thread waits on an mbarrier nothing arrives at; the bounded wait expires
+// and the timeout lands in the status word like any kernel's expired wait.
+__global__ void selftest_timeout_kernel(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* abort_flag = &abort_word;
+    if (!mbar_wait_or_abort(&bar, 0, abort_flag, 99)) publish_abort(abort_flag, status);
+  }
+}
+
 }  // namespace laga
 
 using namespace laga;
@@ -377,6 +394,22 @@ laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, co
   }
   const bool bf = desc->dtype == LAGA_DTYPE_BF16;
   return from_launch(simt_reconstruct(d, bf, c_kv, W_UK, W_UV, k_nope, v, !bf, s));
+}
+
+laga_status laga_mla_selftest_timeout(laga_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* status = device_status_ptr();
+  if (status == nullptr) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "device status word unavailable");
+    return LAGA_ERR_CUDA;
+  }
+  selftest_timeout_kernel<<<1, 32, 0, s>>>(status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "selftest launch: %s", cudaGetErrorString(e));
+    return LAGA_ERR_CUDA;
+  }
+  return LAGA_OK;
 }
 
 laga_status laga_mla_check(laga_stream_t stream) {

@@ -26,7 +26,7 @@ FLAG_REUSE_KV = 1
 
 EXPORTS = ("laga_mla_fwd_workspace_size", "laga_mla_bwd_workspace_size", "laga_mla_fwd", "laga_mla_bwd",
            "laga_mla_reconstruct", "laga_mla_check", "laga_status_string", "laga_mla_last_error",
-           "laga_mla_version")
+           "laga_mla_version", "laga_mla_selftest_timeout")
 
 
 class LagaDesc(ctypes.Structure):
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
     L.laga_mla_reconstruct.restype = st
     L.laga_mla_check.argtypes = [vp]
     L.laga_mla_check.restype = st
+    L.laga_mla_selftest_timeout.argtypes = [vp]
+    L.laga_mla_selftest_timeout.restype = st
     L.laga_status_string.argtypes = [st]
     L.laga_status_string.restype = ctypes.c_char_p
     L.laga_mla_last_error.argtypes = []
@@ -210,6 +212,13 @@ def check(device=None) -> None:
     """laga_mla_check on the current stream: raise on a device-side timeout or CUDA error."""
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     _raise_if(lib().laga_mla_check(_stream(dev)))
+
+
+def selftest_timeout(device=None) -> None:
+    """laga_mla_selftest_timeout on the current stream: enqueue a kernel whose
+    bounded wait expires (about 2 s); the next check() raises LAGA_ERR_TIMEOUT."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _raise_if(lib().laga_mla_selftest_timeout(_stream(dev)))
 
 
 @dataclass
