@@ -257,7 +257,7 @@ def shard_inputs(name: str, seed: int):
     x = make_inputs(full, seed)
     xs = []
     for p in shards:
-        rows = slice(p.q_offset, p.q_offset + p.Sq)
+        rows = np.concatenate([np.arange(off, off + n) for _, n, off in p.segments()])
         xs.append({k: (np.ascontiguousarray(v[:, rows]) if k in ("q", "dout") else v) for k, v in x.items()})
     return shards, xs
 

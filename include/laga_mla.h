@@ -118,6 +118,15 @@ typedef struct {
   int32_t dtype;     /* laga_dtype */
   int32_t variant;   /* laga_variant */
   int32_t flags;     /* bitwise OR of laga_flags (0 = none) */
+  /* Two-segment query shard (zigzag sequence parallelism: rank r holds chunks r and
+   * 2*SP-1-r of the sequence, which evens out the causal work across ranks).
+   * q_split = 0: one segment, rows i at q_offset + i (q_offset2 ignored).
+   * 0 < q_split < sq: rows i < q_split sit at q_offset + i, rows i >= q_split at
+   * q_offset2 + (i - q_split). q_split must be a multiple of 128, and the call must
+   * take the tensor-core materialize path (bf16, the supported dims; AUTO picks it).
+   * Causal shards need q_offset + q_split <= skv and q_offset2 + sq - q_split <= skv. */
+  int64_t q_split;
+  int64_t q_offset2;
 } laga_mla_desc;
 
 /* Descriptor flags.

@@ -31,6 +31,16 @@ class Problem:
     causal: bool = True
     dtype: str = "bf16"  # "bf16" or "f32"
     name: str = ""
+    # Two-segment (zigzag) shard: q_split > 0 puts rows [q_split, Sq) at
+    # positions q_offset2, q_offset2 + 1, ...; rows [0, q_split) stay at q_offset + i.
+    q_split: int = 0
+    q_offset2: int = 0
+
+    def segments(self):
+        """(first local row, rows, first absolute position) of each query segment."""
+        if self.q_split <= 0:
+            return [(0, self.Sq, self.q_offset)]
+        return [(0, self.q_split, self.q_offset), (self.q_split, self.Sq - self.q_split, self.q_offset2)]
 
     @property
     def d_qk(self) -> int:
@@ -39,13 +49,13 @@ class Problem:
     @property
     def skv_eff(self) -> int:
         """Latent rows any query of the shard can see."""
-        return self.q_offset + self.Sq if self.causal else self.S
+        return max(off + n for _, n, off in self.segments()) if self.causal else self.S
 
     @property
     def pairs(self) -> int:
         """Visible (query, key) pairs summed over the batch."""
         if self.causal:
-            return self.B * (self.Sq * self.q_offset + self.Sq * (self.Sq + 1) // 2)
+            return self.B * sum(n * off + n * (n + 1) // 2 for _, n, off in self.segments())
         return self.B * self.Sq * self.S
 
     def flops_fwd(self) -> int:
@@ -84,6 +94,15 @@ def dsv3_rank(r: int, sp: int = 8, seq: int = 16384, n_h: int = 128) -> Problem:
 DSV3_LAST_RANK = dsv3_rank(7)
 
 
+def dsv3_zigzag_rank(r: int, sp: int = 8, seq: int = 16384, n_h: int = 128) -> Problem:
+    """One zigzag SP shard: the sequence cut into 2*sp chunks, rank r holding
+    chunks r and 2*sp-1-r, so every rank sees the same number of (query, key) pairs."""
+    c = seq // (2 * sp)
+    return Problem(B=1, Sq=2 * c, S=seq, n_h=n_h, d_c=512, d_nope=128, d_rope=64, d_v=128,
+                   q_offset=c * r, causal=True, dtype="bf16", q_split=c, q_offset2=c * (2 * sp - 1 - r),
+                   name=f"dsv3_sp{sp}_zigzag_rank{r}_S{seq}_h{n_h}")
+
+
 def sweep_points():
     """Last-rank SP=8 shards over sequence length and head count."""
     for seq in (4096, 8192, 16384, 32768):
@@ -92,9 +111,10 @@ def sweep_points():
 
 
 NAMED = {p.name: p for p in [TINY_F32, MID_BF16] + [dsv3_rank(r) for r in range(8)]
-         + list(sweep_points())}
+         + [dsv3_zigzag_rank(r) for r in range(8)] + list(sweep_points())}
 
 # Workloads made of several shards run back to back in one step: every SP=8
 # rank of the DeepSeek-V3 layer in turn (q_offset = 2048 r), i.e. the whole
 # 16384-token sequence's attention block as eight rank-local calls.
-GROUPS = {"dsv3_sp8_all_ranks_S16384_h128": [dsv3_rank(r) for r in range(8)]}
+GROUPS = {"dsv3_sp8_all_ranks_S16384_h128": [dsv3_rank(r) for r in range(8)],
+          "dsv3_sp8_zigzag_all_ranks_S16384_h128": [dsv3_zigzag_rank(r) for r in range(8)]}

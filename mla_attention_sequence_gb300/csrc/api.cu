@@ -5,6 +5,7 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -95,8 +96,17 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
     *st = fail(LAGA_ERR_INVALID_ARG, "sizes must be positive (d_rope >= 0, q_offset >= 0)%s");
     return Path::Invalid;
   }
-  if (x.causal && x.q_offset + x.sq > x.skv) {
+  const bool two_seg = x.q_split != 0;
+  if (two_seg && (x.q_split < 0 || x.q_split >= x.sq || x.q_split % 128 != 0 || x.q_offset2 < 0)) {
+    *st = fail(LAGA_ERR_INVALID_ARG, "q_split must be 0 or a multiple of 128 in (0, sq), q_offset2 >= 0%s");
+    return Path::Invalid;
+  }
+  if (x.causal && x.q_offset + (two_seg ? x.q_split : x.sq) > x.skv) {
     *st = fail(LAGA_ERR_INVALID_ARG, "causal shard needs q_offset + sq <= skv%s");
+    return Path::Invalid;
+  }
+  if (x.causal && two_seg && x.q_offset2 + (x.sq - x.q_split) > x.skv) {
+    *st = fail(LAGA_ERR_INVALID_ARG, "causal shard needs q_offset2 + sq - q_split <= skv%s");
     return Path::Invalid;
   }
   const int64_t lim = int64_t(1) << 30;
@@ -122,9 +132,14 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
   d->d_rope = static_cast<int>(x.d_rope);
   d->d_v = static_cast<int>(x.d_v);
   d->q_offset = static_cast<int>(x.q_offset);
+  d->q_split = two_seg ? static_cast<int>(x.q_split) : 0;
+  d->q_offset2 = two_seg ? static_cast<int>(x.q_offset2) : 0;
   d->causal = x.causal != 0;
   d->scale = x.softmax_scale > 0.f ? x.softmax_scale : 1.0f / std::sqrt(static_cast<float>(x.d_nope + x.d_rope));
-  d->skv_eff = d->causal ? d->q_offset + d->Sq : d->S;
+  // latent rows any query can see: the furthest position of either segment, plus one
+  d->skv_eff = d->causal ? (two_seg ? std::max(d->q_offset + d->q_split, d->q_offset2 + d->Sq - d->q_split)
+                                    : d->q_offset + d->Sq)
+                         : d->S;
   d->skv_pad = static_cast<int>(align_up(static_cast<size_t>(d->skv_eff), 128));
   d->sq_pad = static_cast<int>(align_up(static_cast<size_t>(d->Sq), 128));
 
@@ -137,6 +152,10 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
   if (!want_simt && x.variant != LAGA_VARIANT_AUTO && !tc_ok) {
     *st = fail(LAGA_ERR_UNSUPPORTED,
                "tensor-core variants need bf16 with d_c=512, d_nope=d_v=128, d_rope=64%s");
+    return Path::Invalid;
+  }
+  if (two_seg && (want_simt || !tc_ok || x.variant == LAGA_VARIANT_FUSED_RECON)) {
+    *st = fail(LAGA_ERR_UNSUPPORTED, "two query segments need the tensor-core materialize path%s");
     return Path::Invalid;
   }
   if (x.variant == LAGA_VARIANT_FUSED_RECON) {
@@ -476,6 +495,6 @@ int laga_mla_profile_read(const char** names, float* ms, int max) {
   return n;
 }
 
-int laga_mla_version(void) { return 100; }
+int laga_mla_version(void) { return 200; }
 
 }  // extern "C"

@@ -69,6 +69,7 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return 8u * k + 16u * (k
 struct Params {
   int* status;
   int Sq, S, n_h, q_offset, causal, skv_pad, sq_pad;
+  int q_split, q_offset2;  // second query segment (q_split = 0: none)
   int successor;  // linear block distance to the CTA that will next run on this SM (the SM count)
   float scale, scale_log2;
   const float* lse2;
@@ -110,8 +111,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int kv0 = blockIdx.x * BKV;  // low key tiles see the most queries: launched first
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int first_qt = p.causal ? max(0, kv0 - p.q_offset) / BQ : 0;
-  const int n_qt = (p.Sq + BQ - 1) / BQ - first_qt;
+  // The query tiles that see this key tile: a suffix of each segment's tiles,
+  // walked segment 0 first. Step i of the walk is query tile qtile(i).
+  const int nq = (p.Sq + BQ - 1) / BQ;
+  const int seg_tiles = p.q_split > 0 ? p.q_split / BQ : nq;  // tiles of the first segment
+  const int first0 = p.causal ? min(seg_tiles, max(0, kv0 - p.q_offset) / BQ) : 0;
+  const int first1 = p.q_split > 0 ? seg_tiles + (p.causal ? min(nq - seg_tiles, max(0, kv0 - p.q_offset2) / BQ) : 0)
+                                   : nq;
+  const int n0 = seg_tiles - first0;
+  const int n_qt = n0 + (nq - first1);
+  auto qtile = [&](int i) { return i < n0 ? first0 + i : first1 + (i - n0); };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -171,7 +180,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_prefetch_2d(&mV, nh * 128, nrow);
           tma_prefetch_2d(&mV, nh * 128 + 64, nrow);
           const int nfirst = p.causal ? max(0, nkv0 - p.q_offset) / BQ : 0;
-          const int nq = (p.Sq + BQ - 1) / BQ;
           for (int k = nfirst; k < nfirst + 2 && k < nq; ++k) {
             tma_prefetch_3d(&mQ, nh * 192, k * BQ, nbb);
             tma_prefetch_3d(&mQ, nh * 192 + 64, k * BQ, nbb);
@@ -186,7 +194,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int s = i % NSTAGE;
         if (!mbar_wait_or_abort(&q_empty[s], ((i / NSTAGE) & 1) ^ 1, abort_flag, 51)) break;
         LAGA_TRACE_POINT(dkdv, 20, i);
-        const int q0 = (first_qt + i) * BQ;
+        const int q0 = qtile(i) * BQ;
         uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
         float* rows = reinterpret_cast<float*>(smem + OFF_ROWV) + s * 2 * BQ;
         mbar_arrive_expect_tx(&q_full[s], STAGE_BYTES + 2 * ROWV_BYTES);
@@ -335,8 +343,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quarter * 32 + lane;
     const int kv = kv0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // local queries i >= q_min see this key (causal); non-causal: the key must exist
-    const int q_min = p.causal ? kv - p.q_offset : (kv < p.S ? 0 : 0x7fffffff);
+    // local queries i >= q_min see this key (causal; per segment); non-causal: the key must exist
+    const int q_min0 = p.causal ? kv - p.q_offset : (kv < p.S ? 0 : 0x7fffffff);
+    const int q_min1 = p.causal ? kv - p.q_offset2 + p.q_split : q_min0;
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
       bool w = true;
@@ -347,7 +356,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     for (int i = 0; i < n_qt; ++i) {
       const int s = i % NSTAGE;
-      const int qc = (first_qt + i) * BQ + 32 * half;  // this thread's first query column
+      const int qt = qtile(i);
+      const int qc = qt * BQ + 32 * half;  // this thread's first query column
+      const int q_min = qt < seg_tiles ? q_min0 : q_min1;
       if (!warp_wait(&q_full[s], (i / NSTAGE) & 1, 61)) { ok = false; break; }
       if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, 62)) { ok = false; break; }
       if (lane == 0) LAGA_TRACE_POINT(dkdv, 10, i);
@@ -557,6 +568,8 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
   p.S = d.S;
   p.n_h = d.n_h;
   p.q_offset = d.q_offset;
+  p.q_split = d.q_split;
+  p.q_offset2 = d.q_offset2;
   p.causal = d.causal ? 1 : 0;
   p.skv_pad = d.skv_pad;
   p.sq_pad = d.sq_pad;

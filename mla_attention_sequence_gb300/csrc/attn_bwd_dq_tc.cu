@@ -57,6 +57,7 @@ constexpr uint32_t SOFTMAX_WARPS = 8;
 struct Params {
   int* status;
   int Sq, S, n_h, q_offset, causal, skv_pad, sq_pad, n_q_tiles;
+  int q_split, q_offset2;  // second query segment (q_split = 0: none)
   float scale, scale_log2;
   const float* lse2;
   const float* delta;
@@ -69,8 +70,14 @@ struct Params {
 // overwrites dP values the other warpgroup has not read yet.
 __device__ __forceinline__ uint32_t packed_col(int k) { return 8u * (k & 3) + 64u * (k >> 2); }
 
+// Absolute position of local query row i (a query tile never straddles the
+// segments: q_split is a multiple of the tile height).
+__device__ __forceinline__ int q_pos(const Params& p, int i) {
+  return (p.q_split > 0 && i >= p.q_split) ? p.q_offset2 + (i - p.q_split) : p.q_offset + i;
+}
+
 __device__ __forceinline__ int n_kv_tiles(const Params& p, int t) {
-  const int last = p.causal ? p.q_offset + min(p.Sq, (t + 1) * BQ) - 1 : p.S - 1;
+  const int last = p.causal ? q_pos(p, min(p.Sq, (t + 1) * BQ) - 1) : p.S - 1;
   return last / BKV + 1;
 }
 
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quarter * 32 + lane;
     const int q_row = t * BQ + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int limit = p.causal ? p.q_offset + q_row : p.S - 1;  // last visible key
+    const int limit = p.causal ? q_pos(p, q_row) : p.S - 1;  // last visible key
     const long long roff = (static_cast<long long>(b) * p.n_h + h) * p.sq_pad + q_row;
     const float lse2 = p.lse2[roff];  // +inf on padded rows: P = 0 there
     const float Drow = p.delta[roff];
@@ -426,6 +433,8 @@ LaunchResult tc_attn_bwd_dq(const Dims& d, const bf16* q, const bf16* k_rope, co
   p.S = d.S;
   p.n_h = d.n_h;
   p.q_offset = d.q_offset;
+  p.q_split = d.q_split;
+  p.q_offset2 = d.q_offset2;
   p.causal = d.causal ? 1 : 0;
   p.skv_pad = d.skv_pad;
   p.sq_pad = d.sq_pad;

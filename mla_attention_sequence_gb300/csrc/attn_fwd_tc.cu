@@ -60,13 +60,20 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 struct FwdParams {
   int* status;  // device status word (timeouts)
   int Sq, S, n_h, q_offset, causal, skv_pad, n_q_tiles;
+  int q_split, q_offset2;  // second query segment (q_split = 0: none)
   float scale_log2;  // softmax scale * log2(e), > 0
   bf16* out;
   float* lse;
 };
 
+// Absolute position of local query row i (a query tile never straddles the
+// segments: q_split is a multiple of the tile height).
+__device__ __forceinline__ int q_pos(const FwdParams& p, int i) {
+  return (p.q_split > 0 && i >= p.q_split) ? p.q_offset2 + (i - p.q_split) : p.q_offset + i;
+}
+
 __device__ __forceinline__ int n_kv_tiles(const FwdParams& p, int t) {
-  const int last = p.causal ? p.q_offset + min(p.Sq, (t + 1) * BQ) - 1 : p.S - 1;
+  const int last = p.causal ? q_pos(p, min(p.Sq, (t + 1) * BQ) - 1) : p.S - 1;
   return last / BKV + 1;
 }
 
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = quarter * 32 + lane;
     const int q_row = t * BQ + r;  // local query index
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int limit = p.causal ? p.q_offset + q_row : p.S - 1;  // last visible key
+    const int limit = p.causal ? q_pos(p, q_row) : p.S - 1;  // last visible key
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY;  // running max of the scaled (log2-domain) scores
     float l_run = 0.f;
@@ -478,6 +485,8 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
   p.S = d.S;
   p.n_h = d.n_h;
   p.q_offset = d.q_offset;
+  p.q_split = d.q_split;
+  p.q_offset2 = d.q_offset2;
   p.causal = d.causal ? 1 : 0;
   p.skv_pad = d.skv_pad;
   p.n_q_tiles = (d.Sq + BQ - 1) / BQ;

@@ -13,6 +13,8 @@ using bf16 = __nv_bfloat16;
 // Problem sizes after validation (all counts fit in int32 on the device side).
 struct Dims {
   int B, Sq, S, n_h, d_c, d_nope, d_rope, d_v, q_offset;
+  // second query segment: rows i >= q_split (0: none) sit at q_offset2 + i - q_split
+  int q_split, q_offset2;
   bool causal;
   float scale;  // softmax scale (natural-log domain)
   int skv_eff;  // latent rows the shard can see

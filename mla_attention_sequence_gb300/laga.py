@@ -35,7 +35,8 @@ class LagaDesc(ctypes.Structure):
                 ("n_h", ctypes.c_int64), ("d_c", ctypes.c_int64), ("d_nope", ctypes.c_int64),
                 ("d_rope", ctypes.c_int64), ("d_v", ctypes.c_int64), ("q_offset", ctypes.c_int64),
                 ("causal", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("variant", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("flags", ctypes.c_int32), ("q_split", ctypes.c_int64),
+                ("q_offset2", ctypes.c_int64)]
 
 
 class LagaError(RuntimeError):
@@ -88,7 +89,8 @@ def _raise_if(status: int):
 
 def make_desc(p: Problem, softmax_scale: float | None = None, variant: str = "auto", flags: int = 0) -> LagaDesc:
     return LagaDesc(p.B, p.Sq, p.S, p.n_h, p.d_c, p.d_nope, p.d_rope, p.d_v, p.q_offset, 1 if p.causal else 0,
-                    float(softmax_scale) if softmax_scale else 0.0, DTYPES[p.dtype], VARIANTS[variant], flags)
+                    float(softmax_scale) if softmax_scale else 0.0, DTYPES[p.dtype], VARIANTS[variant], flags,
+                    p.q_split, p.q_offset2)
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -99,8 +101,10 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset: int, causal: bool) -> Problem:
-    """Infer and check the problem sizes from the input tensors."""
+def problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset: int, causal: bool, q_split: int = 0,
+               q_offset2: int = 0) -> Problem:
+    """Infer and check the problem sizes from the input tensors. q_split > 0 makes
+    rows [q_split, Sq) a second query segment starting at position q_offset2."""
     if q.dim() != 4 or c_kv.dim() != 3 or k_rope.dim() != 3 or W_UK.dim() != 2 or W_UV.dim() != 2:
         raise ValueError("expected q [B,Sq,n_h,d_qk], c_kv [B,S,d_c], k_rope [B,S,d_rope], W [d_c, n_h*d]")
     B, Sq, n_h, d_qk = q.shape
@@ -124,7 +128,8 @@ def problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset: int, causal: bool) -> Prob
         if not t.is_contiguous():
             raise ValueError("inputs must be contiguous")
     return Problem(B=B, Sq=Sq, S=S, n_h=n_h, d_c=d_c, d_nope=d_nope, d_rope=d_rope, d_v=d_v,
-                   q_offset=int(q_offset), causal=bool(causal), dtype=dt)
+                   q_offset=int(q_offset), causal=bool(causal), dtype=dt, q_split=int(q_split),
+                   q_offset2=int(q_offset2))
 
 
 def fwd_workspace_bytes(p: Problem, variant: str = "auto") -> int:
@@ -148,9 +153,10 @@ def _workspace(nbytes: int, device, given: torch.Tensor | None) -> torch.Tensor 
 
 
 def fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset: int = 0, causal: bool = True, softmax_scale: float | None = None,
-        variant: str = "auto", workspace: torch.Tensor | None = None, out=None, lse=None):
+        variant: str = "auto", workspace: torch.Tensor | None = None, out=None, lse=None, q_split: int = 0,
+        q_offset2: int = 0):
     """laga_mla_fwd: returns (out [B,Sq,n_h,d_v], lse [B,n_h,Sq] fp32)."""
-    p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal)
+    p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal, q_split, q_offset2)
     d = make_desc(p, softmax_scale, variant)
     L = lib()
     dev = q.device
@@ -167,13 +173,13 @@ def fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset: int = 0, causal: bool = True, sof
 
 def bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, q_offset: int = 0, causal: bool = True,
         softmax_scale: float | None = None, variant: str = "auto", workspace: torch.Tensor | None = None,
-        grads: dict | None = None, reuse_kv: bool = False):
+        grads: dict | None = None, reuse_kv: bool = False, q_split: int = 0, q_offset2: int = 0):
     """laga_mla_bwd: returns dict dq, dc_kv, dk_rope, dW_UK, dW_UV.
 
     reuse_kv=True (LAGA_FLAG_REUSE_KV): `workspace` is the buffer the forward
     ran with, still holding the K_nope/V it rebuilt; the backward reads them
     instead of rebuilding them."""
-    p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal)
+    p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal, q_split, q_offset2)
     for t in (out, lse, dout):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("out, lse and dout must be contiguous CUDA tensors")
@@ -251,7 +257,7 @@ def step(buf: StepBuffers, variant: str = "auto"):
     """One forward + backward pass of the attention block into preallocated buffers."""
     x, p = buf.inputs, buf.p
     fwd(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], p.q_offset, p.causal, None, variant,
-        buf.ws, buf.out, buf.lse)
+        buf.ws, buf.out, buf.lse, p.q_split, p.q_offset2)
     bwd(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], buf.out, buf.lse, x["dout"], p.q_offset, p.causal,
-        None, variant, buf.ws, buf.grads, reuse_kv=buf.ws is not None)
+        None, variant, buf.ws, buf.grads, reuse_kv=buf.ws is not None, q_split=p.q_split, q_offset2=p.q_offset2)
     return buf.out, buf.lse, buf.grads

@@ -69,12 +69,24 @@ def head_key(k_nope_h, k_rope_b):
     return np.concatenate([_f64(k_nope_h), _f64(k_rope_b)], axis=1)
 
 
+def query_positions(sq, q_offset, q_split=0, q_offset2=0):
+    """Absolute position of every local query row. One segment: q_offset + i. A
+    two-segment (zigzag) shard, q_split > 0: rows i < q_split at q_offset + i,
+    rows i >= q_split at q_offset2 + (i - q_split)."""
+    i = np.arange(sq)
+    if q_split <= 0:
+        return q_offset + i
+    return np.where(i < q_split, q_offset + i, q_offset2 + (i - q_split))
+
+
 def visible_mask(rows, n_keys, q_offset, causal):
-    """Which keys each local query row sees: j <= q_offset + i when causal, else all."""
+    """Which keys each local query row sees: j <= position of row i when causal, else
+    all. q_offset is the first row's position (an int) or every row's position."""
     rows = np.asarray(rows)
     if not causal:
         return np.ones((rows.shape[0], n_keys), dtype=bool)
-    return np.arange(n_keys)[None, :] <= (q_offset + rows)[:, None]
+    pos = q_offset + rows if np.isscalar(q_offset) else np.asarray(q_offset)[rows]
+    return np.arange(n_keys)[None, :] <= pos[:, None]
 
 
 def attention_head_forward(q_h, K_h, V_h, q_offset, causal, scale, rows=None):
@@ -140,9 +152,12 @@ def mla_forward_head(q, c_kv, k_rope, W_UK, W_UV, b, h, q_offset, causal, scale=
     return attention_head_forward(q[b, :, h, :], K_h, v, q_offset, causal, scale, rows)
 
 
-def mla_forward(q, c_kv, k_rope, W_UK, W_UV, q_offset=0, causal=True, scale=None):
-    """Forward of the attention block: returns out [B,Sq,n_h,d_v] and lse [B,n_h,Sq] (fp64)."""
+def mla_forward(q, c_kv, k_rope, W_UK, W_UV, q_offset=0, causal=True, scale=None, q_split=0, q_offset2=0):
+    """Forward of the attention block: returns out [B,Sq,n_h,d_v] and lse [B,n_h,Sq] (fp64).
+    q_split > 0: a two-segment shard (rows from q_split on start at position q_offset2)."""
     B, Sq, n_h, _ = q.shape
+    if q_split > 0:
+        q_offset = query_positions(Sq, q_offset, q_split, q_offset2)
     d_v = W_UV.shape[1] // n_h
     out = np.zeros((B, Sq, n_h, d_v))
     lse = np.zeros((B, n_h, Sq))
@@ -186,14 +201,17 @@ def mla_backward_head(q, c_kv, k_rope, W_UK, W_UV, dout, b, h, q_offset, causal,
     }
 
 
-def mla_backward(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset=0, causal=True, scale=None):
+def mla_backward(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset=0, causal=True, scale=None, q_split=0, q_offset2=0):
     """Backward of the attention block for the loss <dout, out>.
 
     Returns dq [B,Sq,n_h,d_qk], dc_kv [B,S,d_c], dk_rope [B,S,d_rope],
     dW_UK [d_c,n_h*d_nope], dW_UV [d_c,n_h*d_v] (all fp64). Latent rows that no
     query of the shard can see get zero gradient, since they enter nothing.
+    q_split > 0: a two-segment shard, as in mla_forward.
     """
     B, Sq, n_h, d_qk = q.shape
+    if q_split > 0:
+        q_offset = query_positions(Sq, q_offset, q_split, q_offset2)
     S, d_c = c_kv.shape[1], c_kv.shape[2]
     d_nope = W_UK.shape[1] // n_h
     d_v = W_UV.shape[1] // n_h

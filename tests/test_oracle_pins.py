@@ -163,6 +163,40 @@ def test_sequence_parallel_shards_match_sp1(sp):
         np.testing.assert_allclose(sums[k], g1[k], rtol=1e-11, atol=1e-12)
 
 
+# --------------------------------------------------------------------------- zigzag shards
+@pytest.mark.parametrize("sp", [2, 4])
+def test_zigzag_shards_match_sp1(sp):
+    """Zigzag sequence parallelism: the sequence cut into 2*sp chunks, rank r holding
+    chunks r and 2*sp-1-r as one two-segment shard. Gathered, the ranks' outputs,
+    LSEs and dq reproduce the SP=1 result row for row, and their latent and weight
+    gradients sum to SP=1's."""
+    S = 16
+    c = S // (2 * sp)
+    p1 = small(B=1, Sq=S, S=S, q_offset=0)
+    x = inputs64(p1, seed=12)
+    out1, lse1 = run_fwd(p1, x)
+    g1 = run_bwd(p1, x)
+    sums = {k: np.zeros_like(g1[k]) for k in ("dc_kv", "dk_rope", "dW_UK", "dW_UV")}
+    for r in range(sp):
+        a, b = c * r, c * (2 * sp - 1 - r)
+        rows = np.r_[a:a + c, b:b + c]
+        q, dout = x["q"][:, rows], x["dout"][:, rows]
+        o, l = oracle.mla_forward(q, x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], a, True, None, c, b)
+        g = oracle.mla_backward(q, x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], dout, a, True, None, c, b)
+        np.testing.assert_allclose(o, out1[:, rows], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(l, lse1[:, :, rows], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(g["dq"], g1["dq"][:, rows], rtol=1e-11, atol=1e-13)
+        for k in sums:
+            sums[k] += g[k]
+    for k in sums:
+        np.testing.assert_allclose(sums[k], g1[k], rtol=1e-11, atol=1e-12)
+
+
+def test_query_positions_of_a_two_segment_shard():
+    np.testing.assert_array_equal(oracle.query_positions(6, 4), [4, 5, 6, 7, 8, 9])
+    np.testing.assert_array_equal(oracle.query_positions(6, 4, 2, 20), [4, 5, 20, 21, 22, 23])
+
+
 # --------------------------------------------------------------------------- finite differences
 def loss(p, x):
     out, _ = run_fwd(p, x)

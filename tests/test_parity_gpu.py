@@ -43,11 +43,13 @@ def np64(t):
 
 def run_gpu(p, x, variant="auto", backward=True):
     t = to_dev(x, p)
-    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal, None, variant)
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal, None, variant,
+                        q_split=p.q_split, q_offset2=p.q_offset2)
     res = {"out": out, "lse": lse}
     if backward:
         res.update(laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset,
-                            p.causal, None, "auto" if variant == "fused_recon" else variant))
+                            p.causal, None, "auto" if variant == "fused_recon" else variant, q_split=p.q_split,
+                            q_offset2=p.q_offset2))
     laga.check(dev())
     return res
 
@@ -55,11 +57,11 @@ def run_gpu(p, x, variant="auto", backward=True):
 def run_oracle(p, x, backward=True):
     x64 = {k: v.astype(np.float64) for k, v in x.items()}
     out, lse = oracle.mla_forward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], p.q_offset,
-                                  p.causal)
+                                  p.causal, None, p.q_split, p.q_offset2)
     ref = {"out": out, "lse": lse}
     if backward:
         ref.update(oracle.mla_backward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
-                                       p.q_offset, p.causal))
+                                       p.q_offset, p.causal, None, p.q_split, p.q_offset2))
     return ref
 
 
@@ -127,6 +129,10 @@ TC_CASES = {
     "single_query_first": small(Sq=1, S=1, q_offset=0),
     "single_query_last": small(Sq=1, S=701, q_offset=700),
     "multi_tile": small(B=1, n_h=2, Sq=384, S=1000, q_offset=600),
+    # two-segment (zigzag) shards: rows from q_split on start at q_offset2
+    "two_segments": small(B=1, n_h=2, Sq=256, S=1024, q_offset=128, q_split=128, q_offset2=768),
+    "two_segments_ragged": small(B=2, n_h=3, Sq=300, S=900, q_offset=0, q_split=128, q_offset2=600),
+    "two_segments_noncausal": small(n_h=2, Sq=256, S=500, causal=False, q_split=128, q_offset2=0),
 }
 
 
@@ -135,6 +141,11 @@ TC_CASES = {
 def test_tensor_core_forward(name, variant):
     p = TC_CASES[name]
     x = make_inputs(p, seed=10)
+    if p.q_split and variant == "fused_recon":  # two segments: materialize path only
+        with pytest.raises(laga.LagaError) as err:
+            run_gpu(p, x, variant, backward=False)
+        assert err.value.status == 2
+        return
     assert_close(run_gpu(p, x, variant, backward=False), run_oracle(p, x, backward=False), TOL["bf16"],
                  tag=f"{name} {variant}")
 
@@ -226,6 +237,43 @@ def test_dsv3_every_rank_shard_sampled(r):
     assert_close(got, want, TOL["bf16"], tag=f"rank {r} head {h}")
     # latent rows beyond the shard's causal prefix get no gradient
     tail = p.q_offset + p.Sq
+    assert not g["dc_kv"][:, tail:].any() and not g["dk_rope"][:, tail:].any()
+
+    def inner(a, b):
+        return float((np64(a) * b).sum())
+    a_q = inner(g["dq"], x64["q"])
+    a_o = inner(out, x64["dout"])
+    scale_ = max(abs(a_q), abs(a_o), 1.0)
+    assert abs(inner(g["dW_UV"], x64["W_UV"]) - a_o) <= 2e-2 * scale_
+    assert abs(inner(g["dW_UK"], x64["W_UK"]) + inner(g["dk_rope"], x64["k_rope"]) - a_q) <= 2e-2 * scale_
+
+
+@pytest.mark.parametrize("r", [0, 7])
+def test_dsv3_zigzag_shard_sampled(r):
+    """Zigzag SP=8 shards of the DeepSeek-V3 layer (rank r holds sequence chunks r and
+    15 - r of 1024 rows), forward and backward at full size: one head against the
+    per-head oracle with the shard's two-segment positions, plus the gradient
+    identities over all heads."""
+    from mla_attention_sequence_gb300.configs import dsv3_zigzag_rank
+    p = dsv3_zigzag_rank(r)
+    x = make_inputs(p, seed=4000 + r)
+    t = to_dev(x, p)
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True,
+                        q_split=p.q_split, q_offset2=p.q_offset2)
+    g = laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True,
+                 q_split=p.q_split, q_offset2=p.q_offset2)
+    laga.check(dev())
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    h = (29 * r + 3) % p.n_h
+    pos = oracle.query_positions(p.Sq, p.q_offset, p.q_split, p.q_offset2)
+    ref = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
+                                   0, h, pos, True)
+    got = {"out": out[0, :, h], "lse": lse[0, h], "dq": g["dq"][0, :, h],
+           "dW_UK": g["dW_UK"][:, h * 128:(h + 1) * 128], "dW_UV": g["dW_UV"][:, h * 128:(h + 1) * 128]}
+    want = {"out": ref["out_h"], "lse": ref["lse_h"], "dq": ref["dq_h"], "dW_UK": ref["dW_UK_h"],
+            "dW_UV": ref["dW_UV_h"]}
+    assert_close(got, want, TOL["bf16"], tag=f"zigzag rank {r} head {h}")
+    tail = p.skv_eff  # latent rows beyond every query's position get no gradient
     assert not g["dc_kv"][:, tail:].any() and not g["dk_rope"][:, tail:].any()
 
     def inner(a, b):
