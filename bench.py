@@ -61,8 +61,8 @@ def load_peaks():
 # for a --set full capture); the kernel's work and both byte streams (K/V and
 # Q/dO tiles in, dK/dV/dK_rope out) scale with the head count, so x2.
 MEASURED_TRAFFIC = {
-    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "42db7bdbfa4f7214",
-                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (634.161152e6 + 757.207040e6)}},
+    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "b118059bbb4b9c64",
+                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (634.095872e6 + 753.251328e6)}},
 }
 
 
