@@ -184,9 +184,10 @@ def oracle_sample(p: Problem, x: dict, heads: list[int]):
     Returns the algorithmic flops of that sample."""
     import oracle
     x64 = x if all(v.dtype == np.float64 for v in x.values()) else {k: v.astype(np.float64) for k, v in x.items()}
+    pos = oracle.query_positions(p.Sq, p.q_offset, p.q_split, p.q_offset2) if p.q_split > 0 else p.q_offset
     for h in heads:
         oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"], 0, h,
-                                 p.q_offset, p.causal)
+                                 pos, p.causal)
     return p.with_(n_h=len(heads), B=1).flops_step()
 
 
