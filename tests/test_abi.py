@@ -74,6 +74,28 @@ def test_invalid_arguments_are_rejected_before_launch(L):
     assert call_fwd(L, desc(Sq=0)) == 1
 
 
+def test_two_segment_shards_are_checked_before_launch(L):
+    def two(q_split, q_offset2, **kw):
+        d = desc(**kw)
+        d.q_split, d.q_offset2 = q_split, q_offset2
+        return d
+    # q_split must be a multiple of 128 inside (0, sq)
+    assert call_fwd(L, two(100, 0)) == 1
+    assert b"q_split" in L.laga_mla_last_error()
+    assert call_fwd(L, two(-128, 0)) == 1
+    assert call_fwd(L, two(desc().sq, 0)) == 1
+    # the second segment must end inside the latent for a causal shard
+    assert call_fwd(L, two(128, desc().skv)) == 1
+    assert b"q_offset2" in L.laga_mla_last_error()
+    # only the tensor-core materialize path takes two segments
+    assert call_fwd(L, two(128, 0, variant="simt")) == 2
+    assert call_fwd(L, two(128, 0, variant="fused_recon")) == 2
+    assert b"two query segments" in L.laga_mla_last_error()
+    # a valid zigzag shard passes the checks and asks for a workspace
+    d = two(128, 0)
+    assert L.laga_mla_fwd_workspace_size(ctypes.byref(d)) > 0
+
+
 def test_unknown_flag_bits_rejected(L):
     d = desc()
     d.flags = 2
