@@ -223,7 +223,9 @@ int laga_mla_profile_read(const char** names, float* ms, int max);
  * word). Returns LAGA_ERR_CUDA if the launch fails, else LAGA_OK. */
 laga_status laga_mla_selftest_timeout(laga_stream_t stream);
 
-/* Library ABI version: major*10000 + minor*100 + patch. */
+/* Library ABI version: major*10000 + minor*100 + patch. 200 (0.2.0): laga_mla_desc
+ * gained q_split and q_offset2 (two-segment query shards); zero them for the
+ * single-segment behaviour of 100. */
 int laga_mla_version(void);
 
 #ifdef __cplusplus
