@@ -179,29 +179,49 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_sample(p: Problem, x: dict, heads: list[int]):
+def oracle_sample(p: Problem, x: dict, heads: list[int], keep: dict | None = None):
     """Run the fp64 oracle's forward+backward for the given heads of batch 0.
-    Returns the algorithmic flops of that sample."""
+    Returns the algorithmic flops of that sample; `keep` (if given) collects each
+    head's results by head index."""
     import oracle
     x64 = x if all(v.dtype == np.float64 for v in x.values()) else {k: v.astype(np.float64) for k, v in x.items()}
     pos = oracle.query_positions(p.Sq, p.q_offset, p.q_split, p.q_offset2) if p.q_split > 0 else p.q_offset
     for h in heads:
-        oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"], 0, h,
-                                 pos, p.causal)
+        g = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"], 0,
+                                     h, pos, p.causal)
+        if keep is not None:
+            keep[h] = g
     return p.with_(n_h=len(heads), B=1).flops_step()
 
 
-def time_oracle(p: Problem, x: dict, budget_s: float = 15.0, max_heads: int = 64):
+def time_oracle(p: Problem, x: dict, budget_s: float = 15.0, max_heads: int = 64, keep: dict | None = None):
     """Time the oracle over as many heads as fit the time budget (at least one)."""
     x = {k: v.astype(np.float64) for k, v in x.items()}
     t0 = time.perf_counter()
     flops = 0
     heads = 0
     while heads < min(max_heads, p.n_h) and (time.perf_counter() - t0) < budget_s:
-        flops += oracle_sample(p, x, [heads])
+        flops += oracle_sample(p, x, [heads], keep)
         heads += 1
     dt = time.perf_counter() - t0
     return flops / dt / 1e12, heads, dt
+
+
+def sampled_errors(p: Problem, buf, ref_heads: dict) -> dict:
+    """max|gpu - oracle| / max|oracle| per output tensor over the oracle's sampled
+    heads of batch 0 (the per-head outputs: out, lse, dq, dW_UK, dW_UV)."""
+    acc = {}
+    for h, g in ref_heads.items():
+        pairs = {"out": (buf.out[0, :, h], g["out_h"]), "lse": (buf.lse[0, h], g["lse_h"]),
+                 "dq": (buf.grads["dq"][0, :, h], g["dq_h"]),
+                 "dW_UK": (buf.grads["dW_UK"][:, h * p.d_nope:(h + 1) * p.d_nope], g["dW_UK_h"]),
+                 "dW_UV": (buf.grads["dW_UV"][:, h * p.d_v:(h + 1) * p.d_v], g["dW_UV_h"])}
+        for k, (a, r) in pairs.items():
+            a = a.float().cpu().numpy().astype(np.float64)
+            e, m = float(np.abs(a - r).max()), float(np.abs(r).max())
+            pe, pm = acc.get(k, (0.0, 0.0))
+            acc[k] = (max(pe, e), max(pm, m))
+    return {k: e / m if m > 0 else e for k, (e, m) in acc.items()}
 
 
 def host_cores():
@@ -303,13 +323,25 @@ def run_ours(args, name: str):
             d[k] = shared[key][1]
         dinps.append(d)
     torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
     bufs = [laga.alloc_step(p, d, args.variant) for p, d in zip(problems, dinps)]
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         for buf in bufs:
             laga.step(buf, args.variant)
+
+    step()
+    torch.cuda.synchronize()
+    # device memory of one step: inputs, outputs, gradients and the one workspace
+    # the forward and backward share (the library allocates nothing itself)
+    mem = {"peak_mem_bytes": int(torch.cuda.max_memory_allocated(dev)),
+           "workspace_bytes": int(sum(b.ws.numel() if b.ws is not None else 0 for b in bufs)),
+           "inputs_bytes": int(sum(t.numel() * t.element_size() for t in {id(v): v for d in dinps
+                                                                             for v in d.values()}.values())),
+           "what": "torch.cuda.max_memory_allocated over staging the inputs, allocating outputs, gradients "
+                   "and workspace, and one forward+backward (the L2 flush buffer is allocated afterwards)"}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     for _ in range(args.warmup):
         step()
@@ -430,22 +462,31 @@ def run_ours(args, name: str):
     if dom in kflops:
         t_step = sum(per_kernel[dom]) / args.steps
         achieved = kflops[dom] / (t_step * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        # The kernel runs a few ms inside a ~9 ms step, in a timed region well under a
+        # second at the maximum SM clock: burst conditions, so the burst peak applies.
+        peak = peaks["bf16_tflops"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "traffic": kernel_traffic(dom, problems[0].name) if len(problems) == 1 else None,
-                "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
+                "peak_kind": f"bf16 dense, burst, {peaks['source']}",
                 "flops_per_launch": kflops[dom] / len(problems), "ms_per_launch": t_step / len(problems),
                 "launches_per_step": len(problems)}
     launches_per_step = {"simt_fwd": 3, "simt_bwd": 10}  # every other timed step is one kernel
     gpu_launches = sum(launches_per_step.get(k, 1) * len(v) for k, v in per_kernel.items())
 
     cpu = None
+    errors = None
+    oracle_s = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, heads, secs = time_oracle(problems[-1], xs[-1], budget_s=args.cpu_budget)
+        ref_heads = {}
+        tf, heads, secs = time_oracle(problems[-1], xs[-1], budget_s=args.cpu_budget, keep=ref_heads)
+        oracle_s = secs
         cpu = {"value": tf, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                "sample": f"fp64 oracle fwd+bwd of {heads} head(s) (of {problems[-1].n_h}) of shard "
                          f"{problems[-1].name}, {secs:.1f} s; TFLOP/s of the sample's algorithmic flops"}
+        # the same heads of the GPU's last step (same inputs) against the oracle
+        errors = sampled_errors(problems[-1], bufs[-1], ref_heads)
+        errors["heads"] = sorted(ref_heads)
 
     if rank == 0:
         cfg = workload_config(problems[-1], {"variant": args.variant})
@@ -467,6 +508,9 @@ def run_ours(args, name: str):
             "gpu_launches": gpu_launches,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "max_err_over_max_ref": errors,
+            "oracle_s": oracle_s,
+            "memory": mem,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -476,12 +520,30 @@ def run_ours(args, name: str):
 
 
 # ---------------------------------------------------------------- forward variants
+def _time_events(fn, steps, flush, stream):
+    """Median CUDA-event time (ms) of fn over `steps` runs, L2 flushed before each."""
+    import torch
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    return float(np.median(times))
+
+
 def run_variant_sweep(args):
-    """Forward of the two K/V variants over the last-rank SP=8 sweep shapes:
-    'materialize' (reconstruction GEMM to HBM + attention) against
-    'fused_recon' (K/V tiles rebuilt inside the attention kernel). Same
-    algorithmic flops for both (attention + one reconstruction of the visible
-    latent prefix); one JSON line per shape and variant."""
+    """The sweep over the last-rank SP=8 shards (sequence length x heads): per shape,
+    forward + backward of the materialised-K/V variant (the path AUTO takes; the
+    backward reuses the forward's K/V), and the forward of both K/V variants:
+    'materialize' (reconstruction GEMM to HBM + attention) against 'fused_recon'
+    (K/V tiles rebuilt inside the attention kernel; forward only, no backward is
+    built for it). Algorithmic flops as in the main line; one JSON line per shape."""
+    import ctypes
+
     import torch
 
     from mla_attention_sequence_gb300 import build as build_mod
@@ -496,8 +558,34 @@ def run_variant_sweep(args):
     for p in sweep_points():
         if args.sweep_filter and args.sweep_filter not in p.name:
             continue
-        x = make_inputs(p, SEED, with_dout=False)
+        x = make_inputs(p, SEED)
         t = {k: torch.from_numpy(v).to(dev).to(torch.bfloat16) for k, v in x.items()}
+        line = {"mode": "sweep", "workload": p.name, "S": p.S, "n_h": p.n_h, "Sq": p.Sq, "q_offset": p.q_offset,
+                "flops_step": p.flops_step(), "flops_fwd": p.flops_fwd()}
+        # forward + backward, materialised K/V (one workspace shared by both calls)
+        buf = laga.alloc_step(p, t, "materialize")
+
+        def step():
+            laga.step(buf, "materialize")
+        for _ in range(args.warmup):
+            step()
+        laga.check(dev)
+        L.laga_mla_profile_enable(1)
+        ms_step = _time_events(step, args.steps, flush, stream)
+        nmax = 16 * args.steps
+        names = (ctypes.c_char_p * nmax)()
+        ms = (ctypes.c_float * nmax)()
+        n = L.laga_mla_profile_read(ctypes.cast(names, ctypes.POINTER(ctypes.c_char_p)), ms, nmax)
+        L.laga_mla_profile_enable(0)
+        per = {}
+        for i in range(min(n, nmax)):
+            per.setdefault(names[i].decode(), []).append(ms[i])
+        line["materialize"] = {"ms_step": ms_step, "tflops_step": p.flops_step() / (ms_step * 1e-3) / 1e12,
+                               "pct_of_bf16_peak": 100.0 * p.flops_step() / (ms_step * 1e-3) / 1e12
+                               / load_peaks()["bf16_tflops"],
+                               "kernels_ms": {k: float(np.median(v)) for k, v in per.items()},
+                               "workspace_bytes": int(buf.ws.numel()) if buf.ws is not None else 0}
+        del buf
         out = torch.empty((p.B, p.Sq, p.n_h, p.d_v), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((p.B, p.n_h, p.Sq), dtype=torch.float32, device=dev)
         for variant in ("materialize", "fused_recon"):
@@ -510,35 +598,124 @@ def run_variant_sweep(args):
             for _ in range(args.warmup):
                 run()
             laga.check(dev)
-            L.laga_mla_profile_enable(1)
-            times = []
-            for _ in range(args.steps):
-                flush.zero_()
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s.record(stream)
-                run()
-                e.record(stream)
-                torch.cuda.synchronize()
-                times.append(s.elapsed_time(e))
-            import ctypes
-            nmax = 16 * args.steps
-            names = (ctypes.c_char_p * nmax)()
-            ms = (ctypes.c_float * nmax)()
-            n = L.laga_mla_profile_read(ctypes.cast(names, ctypes.POINTER(ctypes.c_char_p)), ms, nmax)
-            L.laga_mla_profile_enable(0)
-            per = {}
-            for i in range(min(n, nmax)):
-                per.setdefault(names[i].decode(), []).append(ms[i])
-            t_ms = float(np.median(times))
-            print(json.dumps({"mode": "variant_sweep", "workload": p.name, "S": p.S, "n_h": p.n_h, "Sq": p.Sq,
-                              "variant": variant, "ms_fwd": t_ms,
-                              "tflops_fwd": p.flops_fwd() / (t_ms * 1e-3) / 1e12,
-                              "kernels_ms": {k: float(np.median(v)) for k, v in per.items()},
-                              "workspace_bytes": nbytes}), flush=True)
+            t_ms = _time_events(run, args.steps, flush, stream)
+            key = "materialize" if variant == "materialize" else "fused_recon"
+            line.setdefault(key, {}).update({"ms_fwd": t_ms, "tflops_fwd": p.flops_fwd() / (t_ms * 1e-3) / 1e12,
+                                             "fwd_workspace_bytes": nbytes})
             del ws
-        del t
+        line["fused_recon"]["bwd"] = "not built (forward-only variant)"
+        print(json.dumps(line), flush=True)
+        del t, out, lse
         torch.cuda.empty_cache()
     return 0
+
+
+# ---------------------------------------------------------------- eager (unfused) baseline
+def eager_forward_backward(t: dict, p: Problem, scale: float):
+    """The attention block written as separate library operations, the 'eager'
+    setting: reconstruction matmuls, the RoPE-key concat, QK^T, mask, softmax in
+    fp32, PV, each a separate cuBLAS / PyTorch kernel with its intermediates in
+    HBM, and torch autograd for the backward. bf16 matmuls with fp32 softmax."""
+    import torch
+    B, Sq, n_h, S = p.B, p.Sq, p.n_h, p.skv_eff
+    q = t["q"].detach().requires_grad_()
+    c = t["c_kv"].detach().requires_grad_()
+    kr = t["k_rope"].detach().requires_grad_()
+    wk = t["W_UK"].detach().requires_grad_()
+    wv = t["W_UV"].detach().requires_grad_()
+    k_nope = (c[:, :S] @ wk).view(B, S, n_h, p.d_nope)
+    v = (c[:, :S] @ wv).view(B, S, n_h, p.d_v)
+    k = torch.cat([k_nope, kr[:, :S, None, :].expand(B, S, n_h, p.d_rope)], dim=-1)
+    sc = torch.matmul(q.permute(0, 2, 1, 3), k.permute(0, 2, 3, 1)).float() * scale  # [B, n_h, Sq, S]
+    if p.causal:
+        pos = torch.arange(Sq, device=q.device) + p.q_offset
+        mask = torch.arange(S, device=q.device)[None, :] > pos[:, None]
+        sc = sc.masked_fill(mask, float("-inf"))
+    with torch.no_grad():
+        lse = torch.logsumexp(sc, dim=-1)
+    prob = torch.softmax(sc, dim=-1).to(torch.bfloat16)
+    out = torch.matmul(prob, v.permute(0, 2, 1, 3)).permute(0, 2, 1, 3)
+    out.backward(t["dout"])
+    return out.detach(), lse.detach(), {"dq": q.grad, "dc_kv": c.grad, "dk_rope": kr.grad, "dW_UK": wk.grad,
+                                        "dW_UV": wv.grad}
+
+
+def run_eager(args, name: str):
+    """Times the eager baseline beside the fused path on the same shard and inputs,
+    checks one head of each against the fp64 oracle, and prints one JSON line."""
+    import torch
+
+    from mla_attention_sequence_gb300 import build as build_mod
+    from mla_attention_sequence_gb300 import laga
+
+    build_mod.build()
+    p = NAMED[name]
+    dev = torch.device("cuda", 0)
+    x = make_inputs(p, SEED)
+    t = {k: torch.from_numpy(v).to(dev).to(torch.bfloat16) for k, v in x.items()}
+    scale = 1.0 / float(np.sqrt(p.d_qk))
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    buf = laga.alloc_step(p, t)
+    for _ in range(args.warmup):
+        laga.step(buf)
+    laga.check(dev)
+    ms_fused = _time_events(lambda: laga.step(buf), args.steps, flush, stream)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    res = {}
+
+    def eager():
+        res["r"] = eager_forward_backward(t, p, scale)
+    for _ in range(max(1, args.warmup // 3)):
+        eager()
+    torch.cuda.synchronize()
+    peak_eager = torch.cuda.max_memory_allocated(dev) - base
+    ms_eager = _time_events(eager, max(2, args.steps // 4), flush, stream)
+    # one head of each against the oracle
+    import oracle
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    h = p.n_h - 1
+    g = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"], 0, h,
+                                 p.q_offset, p.causal)
+    eo, el, eg = res["r"]
+
+    def err(a, r):
+        a = a.float().cpu().numpy().astype(np.float64)
+        return float(np.abs(a - r).max() / np.abs(r).max())
+    errs = {}
+    for tag, (o, l, gr) in {"eager": (eo, el, eg), "fused": (buf.out, buf.lse, buf.grads)}.items():
+        errs[tag] = {"out": err(o[0, :, h], g["out_h"]), "lse": err(l[0, h], g["lse_h"]),
+                     "dq": err(gr["dq"][0, :, h], g["dq_h"]),
+                     "dW_UK": err(gr["dW_UK"][:, h * p.d_nope:(h + 1) * p.d_nope], g["dW_UK_h"]),
+                     "dW_UV": err(gr["dW_UV"][:, h * p.d_v:(h + 1) * p.d_v], g["dW_UV_h"])}
+    flops = p.flops_step()
+    print(json.dumps({"mode": "eager_vs_fused", "workload": p.name, "flops_per_step": flops,
+                      "fused": {"ms_step": ms_fused, "tflops": flops / (ms_fused * 1e-3) / 1e12,
+                                "workspace_bytes": int(buf.ws.numel()) if buf.ws is not None else 0},
+                      "eager": {"ms_step": ms_eager, "tflops": flops / (ms_eager * 1e-3) / 1e12,
+                                "peak_extra_bytes": int(peak_eager),
+                                "what": "cuBLAS bf16 matmuls (reconstruction, QK^T, PV), fp32 mask/softmax, "
+                                        "torch autograd backward; intermediates in HBM"},
+                      "speedup_fused_over_eager": ms_eager / ms_fused,
+                      "max_err_over_max_ref_head": {"head": h, **errs}}), flush=True)
+    return 0
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def relaunch(n: int, argv: list) -> int:
+    """Run this script under torch.distributed.run with n local ranks (rendezvous on
+    127.0.0.1); returns its exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 def main(argv=None):
@@ -552,12 +729,23 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant-sweep", action="store_true",
-                    help="time the forward of both K/V variants over the sweep shapes instead")
+                    help="time fwd+bwd (materialised K/V) and the forward of both K/V variants over the sweep "
+                         "shapes instead")
     ap.add_argument("--sweep-filter", default="", help="only sweep shapes whose name contains this string")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the unfused (eager) baseline beside the fused path on --workload instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # --gpus N outside a launcher: start the N ranks (one process per GPU) here
+        return relaunch(args.gpus, sys.argv[1:] if argv is None else list(argv))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; reporting n_gpus={world}", file=sys.stderr)
     if args.variant_sweep:
         return run_variant_sweep(args)
+    if args.eager:
+        return run_eager(args, args.workload)
     if args.impl == "reference":
         p = GROUPS[args.workload][-1] if args.workload in GROUPS else NAMED[args.workload]
         return run_reference(args, p)

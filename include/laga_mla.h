@@ -55,6 +55,11 @@
  *    workspaces and outputs.
  *  - Reproducibility: no kernel uses atomics; every output is produced in a
  *    fixed order, so repeated calls give bitwise-identical results.
+ *  - Device resets: the library caches, per device and CUDA context, the device
+ *    addresses of its module globals (the status word, the static scratch of
+ *    laga_mla_fwd_noalloc); a new context after cudaDeviceReset is detected and
+ *    the addresses are looked up again. Calls must not run while another thread
+ *    resets the device.
  *
  * Supported problems
  * ------------------
@@ -146,23 +151,46 @@ typedef enum { LAGA_FLAG_REUSE_KV = 1 } laga_flags;
 size_t laga_mla_fwd_workspace_size(const laga_mla_desc* desc);
 size_t laga_mla_bwd_workspace_size(const laga_mla_desc* desc);
 
-/* Forward: out [B,Sq,n_h,d_v] (dtype) and lse [B,n_h,Sq] (fp32).
- * All pointers are device pointers. */
+/* Forward of the attention block on one SP rank: out [B,Sq,n_h,d_v] (dtype) and
+ * lse [B,n_h,Sq] (fp32).
+ * Source: the LAGA page's Abstract (weekinpapers, "A Training-Memory Regression in
+ * MLA Sequence Parallelism ..."): each rank rebuilds every head's K and V from the
+ * gathered latent instead of absorbing W_UK into the query, then runs the
+ * explicit form's attention, whose result LAGA reproduces exactly at SP=1. The
+ * RoPE-key concat and the causal rule at the shard's offset are as defined at the
+ * top of this file.
+ * Arguments: q, c_kv, k_rope, W_UK, W_UV are read-only inputs in the layouts
+ * above; out and lse are written in full; workspace is caller-owned scratch of at
+ * least laga_mla_fwd_workspace_size bytes (256-byte aligned) that the call
+ * overwrites. All pointers are device pointers. Errors: LAGA_ERR_INVALID_ARG /
+ * UNSUPPORTED / WORKSPACE before any launch, LAGA_ERR_CUDA if a launch fails. */
 laga_status laga_mla_fwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
                          const void* W_UK, const void* W_UV, void* out, float* lse, void* workspace,
                          size_t workspace_bytes, laga_stream_t stream);
 
-/* Backward of the loss <dout, out>. out and lse are the forward's outputs for
- * the same inputs. Writes dq, dc_kv, dk_rope, dW_UK, dW_UV (all dtype, shapes of
- * their primals). All pointers are device pointers. */
+/* Backward of the attention block for the loss <dout, out>: the gradients a
+ * training step needs (the Abstract's setting is MLA training under sequence
+ * parallelism), through the attention and through the local K/V rebuild.
+ * Source: the LAGA page's Abstract, as for laga_mla_fwd; the softmax gradient is
+ * the textbook one (dS = P o (dP - rowsum(dout o out))).
+ * Arguments: out and lse are the forward's outputs for the same inputs and
+ * descriptor; dout has out's shape. Writes dq, dc_kv, dk_rope, dW_UK, dW_UV in
+ * full (all dtype, shapes of their primals; dW sums over the batch; dc_kv and
+ * dk_rope are this rank's partial sums, which an SP group adds up). workspace:
+ * at least laga_mla_bwd_workspace_size bytes, 256-byte aligned, overwritten
+ * (see LAGA_FLAG_REUSE_KV for sharing it with the forward). All pointers are
+ * device pointers. Errors as for laga_mla_fwd. */
 laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
                          const void* W_UK, const void* W_UV, const void* out, const float* lse,
                          const void* dout, void* dq, void* dc_kv, void* dk_rope, void* dW_UK, void* dW_UV,
                          void* workspace, size_t workspace_bytes, laga_stream_t stream);
 
-/* Step 1 alone (LAGA's local K/V rebuild): k_nope [B,Skv,n_h,d_nope] and
- * v [B,Skv,n_h,d_v] from c_kv, W_UK, W_UV, for all Skv rows. Device pointers.
- * Needs no workspace. */
+/* Step 1 alone, LAGA's local K/V rebuild (the LAGA page's Abstract: per-head K
+ * and V are reconstructed on each rank from the gathered latent):
+ * k_nope [B,Skv,n_h,d_nope] = c_kv . W_UK and v [B,Skv,n_h,d_v] = c_kv . W_UV,
+ * per head, for all Skv rows, written in full. Device pointers; needs no
+ * workspace; only the descriptor's batch, skv, n_h, d_c, d_nope, d_v, dtype and
+ * variant are used. Errors as for laga_mla_fwd. */
 laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
                                  const void* W_UV, void* k_nope, void* v, laga_stream_t stream);
 

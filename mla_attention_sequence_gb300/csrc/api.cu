@@ -38,38 +38,54 @@ laga_status from_launch(const LaunchResult& r) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// ---- opt-in kernel timing: one event pair per launch, events pooled per thread
+// ---- opt-in kernel timing: one event pair per launch, events pooled per thread.
+// Each record keeps the pool indices of its own two events, so a launch whose
+// events could not be created is skipped without shifting the pairs after it.
+struct ProfRecord {
+  const char* name;
+  size_t begin, end;  // indices into pool
+};
 struct Profiler {
   bool on = false;
   std::vector<cudaEvent_t> pool;
-  std::vector<const char*> names;
+  std::vector<ProfRecord> recs;
   size_t used = 0;  // events handed out since the last enable
+  bool open = false;  // a begin was recorded and awaits its end
 };
 thread_local Profiler t_prof;
 
-cudaEvent_t prof_event() {
+// Index of the next free pooled event (created on first use), or -1.
+long prof_event() {
   Profiler& P = t_prof;
   if (P.used == P.pool.size()) {
     cudaEvent_t e = nullptr;
-    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return -1;
     P.pool.push_back(e);
   }
-  return P.pool[P.used++];
+  return static_cast<long>(P.used++);
 }
 
 // Records the start event of a launch named `name` (no-op when disabled).
 void prof_begin(const char* name, cudaStream_t s) {
-  if (!t_prof.on) return;
-  cudaEvent_t e = prof_event();
-  if (e) cudaEventRecord(e, s);
-  t_prof.names.push_back(e ? name : nullptr);
+  Profiler& P = t_prof;
+  P.open = false;
+  if (!P.on) return;
+  const long e = prof_event();
+  if (e < 0 || cudaEventRecord(P.pool[e], s) != cudaSuccess) return;
+  P.recs.push_back(ProfRecord{name, static_cast<size_t>(e), 0});
+  P.open = true;
 }
 
 void prof_end(cudaStream_t s) {
-  if (!t_prof.on) return;
-  if (!t_prof.names.empty() && t_prof.names.back() == nullptr) return;
-  cudaEvent_t e = prof_event();
-  if (e) cudaEventRecord(e, s);
+  Profiler& P = t_prof;
+  if (!P.on || !P.open) return;
+  P.open = false;
+  const long e = prof_event();
+  if (e < 0 || cudaEventRecord(P.pool[e], s) != cudaSuccess) {
+    P.recs.pop_back();  // no end event: drop the record
+    return;
+  }
+  P.recs.back().end = static_cast<size_t>(e);
 }
 
 // Run one launcher between two profiling marks.
@@ -96,6 +112,19 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
     *st = fail(LAGA_ERR_INVALID_ARG, "sizes must be positive (d_rope >= 0, q_offset >= 0)%s");
     return Path::Invalid;
   }
+  // Bound every factor first, so that the products below cannot overflow.
+  const int64_t lim = int64_t(1) << 30;
+  if (x.skv >= lim || x.sq >= lim || x.q_offset >= lim || (x.q_split != 0 && x.q_offset2 >= lim) ||
+      x.batch >= 65536 ||
+      x.n_h >= 65536 || x.d_c >= 65536 || x.d_nope >= 65536 || x.d_rope >= 65536 || x.d_v >= 65536) {
+    *st = fail(LAGA_ERR_UNSUPPORTED, "problem too large%s");
+    return Path::Invalid;
+  }
+  if (x.batch * x.skv * x.n_h * (x.d_nope + x.d_rope + x.d_v) >= (int64_t(1) << 40) ||
+      x.batch * x.sq * x.n_h * (x.d_nope + x.d_rope + x.d_v) >= (int64_t(1) << 40)) {
+    *st = fail(LAGA_ERR_UNSUPPORTED, "problem too large%s");
+    return Path::Invalid;
+  }
   const bool two_seg = x.q_split != 0;
   if (two_seg && (x.q_split < 0 || x.q_split >= x.sq || x.q_split % 128 != 0 || x.q_offset2 < 0)) {
     *st = fail(LAGA_ERR_INVALID_ARG, "q_split must be 0 or a multiple of 128 in (0, sq), q_offset2 >= 0%s");
@@ -107,12 +136,6 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
   }
   if (x.causal && two_seg && x.q_offset2 + (x.sq - x.q_split) > x.skv) {
     *st = fail(LAGA_ERR_INVALID_ARG, "causal shard needs q_offset2 + sq - q_split <= skv%s");
-    return Path::Invalid;
-  }
-  const int64_t lim = int64_t(1) << 30;
-  if (x.batch * x.skv * x.n_h * (x.d_nope + x.d_rope + x.d_v) >= (int64_t(1) << 40) || x.skv >= lim ||
-      x.sq >= lim || x.batch >= 65536 || x.n_h >= 65536) {
-    *st = fail(LAGA_ERR_UNSUPPORTED, "problem too large%s");
     return Path::Invalid;
   }
   if ((x.flags & ~static_cast<int32_t>(LAGA_FLAG_REUSE_KV)) != 0) {
@@ -193,6 +216,22 @@ CuTensorMapEncodeTiled encode_fn() {
   return fn;
 }
 
+
+using CuCtxGetCurrent = CUresult (*)(CUcontext*);
+
+CuCtxGetCurrent ctx_fn() {
+  static CuCtxGetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CuCtxGetCurrent>(p);
+  });
+  return fn;
+}
+
 }  // namespace
 
 void set_last_error(const char* msg) { std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
@@ -209,15 +248,29 @@ int sm_count() {
   return counts[dev];
 }
 
+void* current_context() {
+  CuCtxGetCurrent fn = ctx_fn();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 int* device_status_ptr() {
+  // Cached per device together with the context it was looked up in: a new
+  // primary context (after cudaDeviceReset) reloads the module, and the word
+  // may then sit at another address.
   static int* ptrs[64] = {};
+  static void* ctxs[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (!ptrs[dev] || ctxs[dev] != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) ptrs[dev] = static_cast<int*>(p);
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+    ctxs[dev] = ctx;
   }
   return ptrs[dev];
 }
@@ -473,24 +526,21 @@ const char* laga_mla_last_error(void) { return t_last_error; }
 laga_status laga_mla_profile_enable(int enable) {
   t_prof.on = enable != 0;
   t_prof.used = 0;
-  t_prof.names.clear();
+  t_prof.open = false;
+  t_prof.recs.clear();
   return LAGA_OK;
 }
 
 int laga_mla_profile_read(const char** names, float* ms, int max) {
   const Profiler& P = t_prof;
-  const int n = static_cast<int>(P.names.size());
-  int out = 0;
-  for (int i = 0; i < n && out < max; ++i) {
-    if (P.names[i] == nullptr) continue;
-    if (2 * static_cast<size_t>(i) + 1 >= P.used) break;
-    cudaEvent_t a = P.pool[2 * i], b = P.pool[2 * i + 1];
-    if (cudaEventSynchronize(b) != cudaSuccess) return -1;
+  const int n = static_cast<int>(P.recs.size());
+  for (int i = 0; i < n && i < max; ++i) {
+    const ProfRecord& r = P.recs[i];
+    if (cudaEventSynchronize(P.pool[r.end]) != cudaSuccess) return -1;
     float t = 0.f;
-    if (cudaEventElapsedTime(&t, a, b) != cudaSuccess) return -1;
-    if (names) names[out] = P.names[i];
-    if (ms) ms[out] = t;
-    ++out;
+    if (cudaEventElapsedTime(&t, P.pool[r.begin], P.pool[r.end]) != cudaSuccess) return -1;
+    if (names) names[i] = r.name;
+    if (ms) ms[i] = t;
   }
   return n;
 }

@@ -30,20 +30,26 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device. In host code the
 // symbol's name is only a host-side handle, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached together with the context
+// it was looked up in: should the caller reset the device, the new primary
+// context loads the module afresh and the array may sit elsewhere, so the
+// address is looked up again.
 cudaError_t scratch_address(void** out) {
   static void* addr[64] = {};
+  static void* ctxs[64] = {};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctxs[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     addr[dev] = p;
+    ctxs[dev] = ctx;
   }
   *out = addr[dev];
   return cudaSuccess;

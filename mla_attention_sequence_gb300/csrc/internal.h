@@ -19,7 +19,7 @@ struct Dims {
   float scale;  // softmax scale (natural-log domain)
   int skv_eff;  // latent rows the shard can see
   int skv_pad;  // skv_eff rounded up to the 128-row key tile
-  int sq_pad;   // Sq rounded up to the 64-row query tile of the backward
+  int sq_pad;   // Sq rounded up to 128 (the forward and dq query tile; two 64-row dK/dV query tiles)
   __host__ __device__ int d_qk() const { return d_nope + d_rope; }
 };
 
@@ -34,6 +34,9 @@ struct LaunchResult {
 // Device address of this device's status word (timeouts of bounded waits);
 // nullptr if it cannot be resolved.
 int* device_status_ptr();
+// Handle of the calling thread's current CUDA context (nullptr if none): the key,
+// beside the device number, of the per-device caches of module symbol addresses.
+void* current_context();
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -327,6 +327,51 @@ def test_hand_worked_two_token_example():
                                atol=1e-13)
 
 
+def test_default_scale_is_one_over_root_of_query_key_width():
+    """Reading of the pages' silence on the softmax scale: 1/sqrt(d_nope + d_rope),
+    the width of the concatenated query/key (192 at the DeepSeek-V3 dims, 48 tiny)."""
+    assert O.default_scale(128, 64) == pytest.approx(1.0 / 13.856406460551018, rel=1e-15)  # sqrt(192)
+    assert O.default_scale(32, 16) == pytest.approx(1.0 / 6.928203230275509, rel=1e-15)  # sqrt(48)
+    assert O.default_scale(2, 2) == 0.5
+
+
+def test_hand_worked_example_at_the_default_scale():
+    """Two tokens, one head, d_c = 2, d_nope = d_rope = 2 (so the default scale is
+    1/sqrt(4) = 1/2), d_v = 1, worked by hand with no scale passed.
+
+    c_kv = I, W_UK = [[0, 0], [2 ln 3, 0]]: K_nope = ((0, 0), (2 ln 3, 0)).
+    k_rope = ((0, 1), (0, 0)); W_UV = (2, 6): V = (2, 6).
+    Query 0 = (0, 0, 0, 2) sees key 0 only: s_00 = 1/2 * 2 = 1, out_0 = 2, lse_0 = 1.
+    Query 1 = (1, 0, 0, 0) sees both: scores (0, 1/2 * 2 ln 3) = (0, ln 3), weights
+    (1/4, 3/4): out_1 = 5, lse_1 = ln 4.
+    Backward from dout = 1: ds_1 = (1/4 (2-5), 3/4 (6-5)) = (-3/4, 3/4), ds_0 = 0;
+    dq_1 = 1/2 (-3/4 K_0 + 3/4 K_1) = (3/4 ln 3, 0, 0, -3/8);
+    dK_0 = 1/2 (-3/4) q_1 = (-3/8, 0, 0, 0), dK_1 = (3/8, 0, 0, 0): dk_rope = 0;
+    dW_UK = dK_nope = ((-3/8, 0), (3/8, 0)); dV = (1 + 1/4, 3/4): dW_UV = (5/4, 3/4);
+    dc_kv_0 = (-3/8, 0) W_UK^T + 5/4 (2, 6) = (5/2, 15/2 - 3/4 ln 3),
+    dc_kv_1 = (3/8, 0) W_UK^T + 3/4 (2, 6) = (3/2, 9/2 + 3/4 ln 3).
+    A scale of 1/sqrt(d_nope) (or no scale) moves every one of these numbers."""
+    ln3 = math.log(3.0)
+    x = {
+        "q": np.array([[[[0.0, 0.0, 0.0, 2.0]], [[1.0, 0.0, 0.0, 0.0]]]]),
+        "c_kv": np.array([[[1.0, 0.0], [0.0, 1.0]]]),
+        "k_rope": np.array([[[0.0, 1.0], [0.0, 0.0]]]),
+        "W_UK": np.array([[0.0, 0.0], [2.0 * ln3, 0.0]]),
+        "W_UV": np.array([[2.0], [6.0]]),
+        "dout": np.ones((1, 2, 1, 1)),
+    }
+    out, lse = oracle.mla_forward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], 0, True)
+    np.testing.assert_allclose(out[0, :, 0, 0], [2.0, 5.0], rtol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], [1.0, math.log(4.0)], rtol=1e-14)
+    g = oracle.mla_backward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], x["dout"], 0, True)
+    np.testing.assert_allclose(g["dq"][0, :, 0], [[0.0, 0.0, 0.0, 0.0], [0.75 * ln3, 0.0, 0.0, -0.375]],
+                               atol=1e-14)
+    np.testing.assert_allclose(g["dk_rope"][0], [[0.0, 0.0], [0.0, 0.0]], atol=1e-14)
+    np.testing.assert_allclose(g["dW_UK"], [[-0.375, 0.0], [0.375, 0.0]], atol=1e-14)
+    np.testing.assert_allclose(g["dW_UV"][:, 0], [1.25, 0.75], atol=1e-14)
+    np.testing.assert_allclose(g["dc_kv"][0], [[2.5, 7.5 - 0.75 * ln3], [1.5, 4.5 + 0.75 * ln3]], atol=1e-13)
+
+
 # --------------------------------------------------------------------------- identities
 def inner(a, b):
     return float((np.asarray(a) * np.asarray(b)).sum())
@@ -409,6 +454,10 @@ def _head_key_transposed_rope(k_nope_h, k_rope_b):
         :, :k_nope_h.shape[1] + k_rope_b.shape[1]]
 
 
+def _default_scale_nope_only(d_nope, d_rope):
+    return 1.0 / np.sqrt(d_nope)
+
+
 _ORIG_BWD = O.attention_head_backward
 
 
@@ -419,6 +468,7 @@ def _pins_pass():
         lambda: test_finite_differences_every_input(True, 3),
         lambda: test_torch_autograd_float64(),
         lambda: test_hand_worked_two_token_example(),
+        lambda: test_hand_worked_example_at_the_default_scale(),
     ]
     for c in checks:
         try:
@@ -434,8 +484,25 @@ def _pins_pass():
     ("attention_head_backward", _attention_backward_no_scale_dq),
     ("attention_head_backward", _attention_backward_sign),
     ("head_key", _head_key_transposed_rope),
+    ("default_scale", _default_scale_nope_only),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, target, mutant):
     assert _pins_pass()
     monkeypatch.setattr(O, target, mutant)
     assert not _pins_pass(), f"no pin caught the planted mistake in {target}"
+
+
+# --------------------------------------------------------------------------- multi-process helper
+def test_head_parallel_oracle_helper_matches_the_oracle():
+    """The helper the full-size GPU tests use (heads dealt to spawned workers, each
+    calling the per-head oracle) returns the oracle's own results."""
+    import oracle_heads
+    p = small(B=2, Sq=6, S=11, n_h=5, q_offset=5)
+    x = make_inputs(p, seed=31)
+    got = oracle_heads.full_backward(p, x, workers=2)
+    xs = inputs64(p, seed=31)
+    out, lse = run_fwd(p, xs)
+    ref = run_bwd(p, xs)
+    ref.update(out=out, lse=lse)
+    for k, r in ref.items():
+        np.testing.assert_allclose(got[k], r, rtol=1e-12, atol=1e-14, err_msg=k)

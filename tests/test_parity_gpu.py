@@ -41,27 +41,27 @@ def np64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(p, x, variant="auto", backward=True):
+def run_gpu(p, x, variant="auto", backward=True, scale=None):
     t = to_dev(x, p)
-    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal, None, variant,
+    out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal, scale, variant,
                         q_split=p.q_split, q_offset2=p.q_offset2)
     res = {"out": out, "lse": lse}
     if backward:
         res.update(laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset,
-                            p.causal, None, "auto" if variant == "fused_recon" else variant, q_split=p.q_split,
+                            p.causal, scale, "auto" if variant == "fused_recon" else variant, q_split=p.q_split,
                             q_offset2=p.q_offset2))
     laga.check(dev())
     return res
 
 
-def run_oracle(p, x, backward=True):
+def run_oracle(p, x, backward=True, scale=None):
     x64 = {k: v.astype(np.float64) for k, v in x.items()}
     out, lse = oracle.mla_forward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], p.q_offset,
-                                  p.causal, None, p.q_split, p.q_offset2)
+                                  p.causal, scale, p.q_split, p.q_offset2)
     ref = {"out": out, "lse": lse}
     if backward:
         ref.update(oracle.mla_backward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"],
-                                       p.q_offset, p.causal, None, p.q_split, p.q_offset2))
+                                       p.q_offset, p.causal, scale, p.q_split, p.q_offset2))
     return ref
 
 
@@ -155,6 +155,69 @@ def test_tensor_core_backward(name):
     p = TC_CASES[name]
     x = make_inputs(p, seed=11)
     assert_close(run_gpu(p, x, "materialize"), run_oracle(p, x), TOL["bf16"], tag=name)
+
+
+# ------------------------------------------------------------------ explicit softmax scale
+# Every other case takes the default scale (softmax_scale <= 0). These pass one
+# explicitly: it feeds the exponent scale of all three attention kernels and the
+# final dq / dK scaling, so a wrong or ignored value shows in every output.
+SCALED_CASES = {
+    "tc_ragged_causal": (small(B=2, n_h=3, Sq=200, S=520, q_offset=300), "materialize"),
+    "tc_two_segments": (small(B=2, n_h=3, Sq=300, S=900, q_offset=0, q_split=128, q_offset2=600), "materialize"),
+    "tc_noncausal": (small(n_h=2, Sq=77, S=333, causal=False), "materialize"),
+    "simt_f32": (Problem(B=2, n_h=3, d_c=24, d_nope=8, d_rope=4, d_v=12, dtype="f32", q_offset=5, Sq=11, S=23,
+                         causal=True), "simt"),
+}
+
+
+@pytest.mark.parametrize("scale", [0.05, 0.2])
+@pytest.mark.parametrize("name", list(SCALED_CASES))
+def test_explicit_softmax_scale(name, scale):
+    p, variant = SCALED_CASES[name]
+    x = make_inputs(p, seed=16)
+    assert_close(run_gpu(p, x, variant, scale=scale), run_oracle(p, x, scale=scale), TOL[p.dtype],
+                 tag=f"{name} scale={scale}")
+
+
+def test_explicit_softmax_scale_fused_forward():
+    p = small(B=2, n_h=3, Sq=200, S=520, q_offset=300)
+    x = make_inputs(p, seed=17)
+    assert_close(run_gpu(p, x, "fused_recon", backward=False, scale=0.2),
+                 run_oracle(p, x, backward=False, scale=0.2), TOL["bf16"], tag="fused scale=0.2")
+
+
+def test_explicit_scale_equal_to_default_is_bitwise_default():
+    """softmax_scale = 1/sqrt(192) passed explicitly takes the same arithmetic as the default."""
+    p = small(B=1, n_h=2, Sq=200, S=520, q_offset=300)
+    x = make_inputs(p, seed=18)
+    a = run_gpu(p, x)
+    b = run_gpu(p, x, scale=float(np.float32(1.0) / np.sqrt(np.float32(192.0))))
+    for k in KEYS:
+        assert torch.equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------------ all 128 heads, element by element
+def test_full_head_count_shard_every_output():
+    """n_h = 128, the DeepSeek-V3 head count, on a shard small enough for the whole
+    oracle: every output element by element, including the two cross-head
+    reductions (dc_kv's contraction over n_h * 256 = 32768 and dk_rope's sum over
+    128 heads)."""
+    p = small(B=1, n_h=128, Sq=512, S=2048, q_offset=1536)
+    x = make_inputs(p, seed=19)
+    assert_close(run_gpu(p, x), run_oracle(p, x), TOL["bf16"], tag="n_h=128 shard")
+
+
+def test_dsv3_last_rank_full_oracle_every_output():
+    """The DeepSeek-V3 SP=8 last-rank shard (the benchmark's launch configuration):
+    all seven outputs element by element against the full 128-head fp64 oracle.
+    The oracle's heads are split over worker processes; each worker runs the
+    per-head oracle on its heads and adds up their dc_kv / dk_rope contributions."""
+    import oracle_heads
+    p = DSV3_LAST_RANK
+    x = make_inputs(p, seed=2007)
+    ref = oracle_heads.full_backward(p, x)
+    got = run_gpu(p, x)
+    assert_close(got, ref, TOL["bf16"], tag="dsv3 last rank, full oracle")
 
 
 def test_mid_config_full_parity():

@@ -4,13 +4,17 @@ Such callers (a plug-in whose host framework owns all device memory, a runtime
 with a fixed memory budget, a C caller without an allocator) cannot pass a
 workspace, so this entry point keeps the forward's scratch in a static device
 array of the library. The test calls it through the C ABI twice in a row, on
-two different problems, and checks each result against laga_mla_fwd (the
-entry point with a caller workspace) within the bf16 tolerance the parity
-tests use: max|diff| <= 2e-2 * max|reference|. This file is collected last.
+two different problems, the larger one second (so that a region the second
+call failed to write would still hold the first call's data or zeros, not the
+right values), and checks each result against laga_mla_fwd (the entry point
+with a caller workspace). Both run the same kernels in the same order on the
+same inputs, and the library's kernels are bitwise reproducible, so the results
+must be bitwise equal; that is a stricter check than the bf16 tolerance the
+parity tests use (max|diff| <= 2e-2 * max|reference|), which therefore holds
+too. This file is collected last.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -20,7 +24,6 @@ from mla_attention_sequence_gb300.synth import make_inputs
 
 pytestmark = pytest.mark.gpu
 
-TOL = 2e-2
 
 
 def _lib():
@@ -47,19 +50,14 @@ def _noalloc_forward(L, p, t):
     return out, lse
 
 
-def _close(a, b):
-    a = a.float().cpu().numpy().astype(np.float64)
-    b = b.float().cpu().numpy().astype(np.float64)
-    return np.abs(a - b).max() <= TOL * np.abs(b).max()
-
-
 def test_noalloc_forward_matches_workspace_forward_twice():
     L = _lib()
     dev = torch.device("cuda", 0)
     problems = [
-        Problem(B=1, Sq=384, S=1000, n_h=4, d_c=512, d_nope=128, d_rope=64, d_v=128, q_offset=600, causal=True,
-                dtype="bf16"),
         Problem(B=2, Sq=200, S=520, n_h=3, d_c=512, d_nope=128, d_rope=64, d_v=128, q_offset=300, causal=True,
+                dtype="bf16"),
+        # larger second: 32 MiB of the 64 MiB array
+        Problem(B=1, Sq=1000, S=4096, n_h=16, d_c=512, d_nope=128, d_rope=64, d_v=128, q_offset=3000, causal=True,
                 dtype="bf16"),
     ]
     for i, p in enumerate(problems):
@@ -68,8 +66,10 @@ def test_noalloc_forward_matches_workspace_forward_twice():
         ref_out, ref_lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal)
         out, lse = _noalloc_forward(L, p, t)
         torch.cuda.synchronize()
-        assert _close(out, ref_out), f"call {i}: out differs"
-        assert _close(lse, ref_lse), f"call {i}: lse differs"
+        assert laga.fwd_workspace_bytes(p) <= 64 * 1024 * 1024
+        assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+        assert torch.equal(out, ref_out), f"call {i}: out differs"
+        assert torch.equal(lse, ref_lse), f"call {i}: lse differs"
 
 
 def test_noalloc_rejects_problems_beyond_the_static_array():
