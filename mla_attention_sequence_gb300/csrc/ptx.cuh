@@ -316,6 +316,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -472,7 +484,7 @@ __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* sta
 // (warp, step, tag), with plain stores; a debug export copies the array out.
 // Release builds compile every trace point to nothing.
 #ifdef LAGA_TRACE
-#define LAGA_TRACE_WARPS 16
+#define LAGA_TRACE_WARPS 32
 #define LAGA_TRACE_STEPS 512
 #define LAGA_TRACE_TAGS 32
 #define LAGA_TRACE_CAP (LAGA_TRACE_WARPS * LAGA_TRACE_STEPS * LAGA_TRACE_TAGS)
@@ -501,7 +513,8 @@ __device__ __forceinline__ void publish_abort(volatile int* abort_flag, int* sta
   }
 #define LAGA_TRACE_POINT(name, tag, step)                                                \
   do {                                                                                   \
-    if (blockIdx.x == 0 && blockIdx.y == LAGA_TRACE_BY && blockIdx.z == 0 && (step) < LAGA_TRACE_STEPS) \
+    if (blockIdx.x == 0 && blockIdx.y == LAGA_TRACE_BY && blockIdx.z == 0 && (step) >= 0 &&              \
+        (step) < LAGA_TRACE_STEPS && (threadIdx.x >> 5) < LAGA_TRACE_WARPS)                               \
       g_trace_##name[((threadIdx.x >> 5) * LAGA_TRACE_STEPS + (step)) * LAGA_TRACE_TAGS + (tag)] = \
           clock64();                                                                     \
   } while (0)
