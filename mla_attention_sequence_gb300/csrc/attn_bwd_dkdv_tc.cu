@@ -24,9 +24,16 @@
 //               costs it next to nothing.
 //   warps 2..9  two warpgroups; each thread owns one key row (TMEM lane) and
 //               half of the 64 query columns: P^T, dS^T, and half the epilogue
-// TMEM columns: dV [0,128), dK [128,320), S^T/P^T x2 [320,448), dP^T/dS^T [448,512).
-// MMA order S(0) dP(0) S(1) | dV(i) dK(i) dP(i+1) S(i+2) | ... keeps the next
-// query tile's products queued behind the current one's.
+// TMEM columns: dV [0,128), dK [128,320), S^T x2 [320,448), dP^T [448,512).
+// Step i packs P^T(i) AND dS^T(i) into its own S^T buffer (P^T over the first
+// 16 of each warpgroup's 32 score columns, dS^T over the other 16), so the dP^T
+// columns are free as soon as the softmax has read dP^T(i) into registers.
+// MMA order S(0) dP(0) S(1) | dV(i) dP(i+1) dK(i) S(i+2) | ...: dP(i+1) no longer
+// waits behind dK(i), which leaves every hand-off (P^T, dP^T read, dS^T) most of
+// a step of slack instead of a few hundred cycles (measured on GB300: with the
+// order dV(i) dK(i) dP(i+1) S(i+2) and dS^T over dP^T, the MMA warp waited
+// ~400 cycles per step at the P^T and dS^T hand-offs, 1820 cycles per step
+// against 1600 of tensor work).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -62,9 +69,11 @@ constexpr int WAITER_WARP = 10;
 constexpr int HANDOFF_BAR = 1;  // named barrier of warp 1 and the waiter (64 threads)
 constexpr uint32_t SOFTMAX_WARPS = 8;
 
-// TMEM column of packed bf16 chunk k (16 queries) of a 64-query tile: the two
-// warpgroups pack their halves at columns [0,16) and [32,48).
+// TMEM column (within a step's S^T buffer) of packed bf16 chunk k (16 queries)
+// of P^T: the two warpgroups pack their halves at [0,16) and [32,48); of dS^T:
+// at [16,32) and [48,64), the score columns each warpgroup has read already.
 __device__ __forceinline__ uint32_t packed_col(int k) { return 8u * k + 16u * (k >> 1); }
+__device__ __forceinline__ uint32_t packed_col_ds(int k) { return 16u + 8u * k + 16u * (k >> 1); }
 
 struct Params {
   int* status;
@@ -99,11 +108,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // P^T of step i+1 can be ready before the MMA thread has seen step i's, so
   // p_full alternates between two barriers (one phase of each per two steps).
   uint64_t* p_full = bars + 10;  // [2]
-  uint64_t* ds_full = bars + 12;
+  // dS^T(i) can complete before the waiter has seen dS^T(i-1) (dP(i) is issued
+  // before that hand-off), so ds_full alternates between two barriers too.
+  auto ds_full = [bars](int i) { return (i & 1) ? bars + 17 : bars + 12; };
   uint64_t* acc_done = bars + 13;
   uint64_t* drain = bars + 14;
   uint64_t* epi_full = bars + 15;  // epilogue tiles staged in shared memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* dp_free = bars + 16;   // dP^T(i) read into registers: dP(i+1) may overwrite it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -133,7 +145,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(dp_full, 1);
     mbar_init(&p_full[0], SOFTMAX_WARPS);
     mbar_init(&p_full[1], SOFTMAX_WARPS);
-    mbar_init(ds_full, SOFTMAX_WARPS);
+    mbar_init(ds_full(0), SOFTMAX_WARPS);
+    mbar_init(ds_full(1), SOFTMAX_WARPS);
+    mbar_init(dp_free, SOFTMAX_WARPS);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     mbar_init(epi_full, SOFTMAX_WARPS);
@@ -217,9 +231,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == WAITER_WARP) {
     // The waiter walks the MMA warp's waits in the same order: kv_full, then per
-    // step i p_full(i), ds_full(i) (i >= 0) and q_full(i+2) (i + 2 < n). Each wait
-    // ends at the named barrier; a failed wait (timeout or abort) is ANDed in, and
-    // both warps leave their loops at the same hand-off.
+    // step i p_full(i), dp_free(i) (i + 1 < n), ds_full(i) (i >= 0) and q_full(i+2)
+    // (i + 2 < n). Each wait ends at the named barrier; a failed wait (timeout or
+    // abort) is ANDed in, and both warps leave their loops at the same hand-off.
     auto handoff = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
       const bool w = warp_wait_or_abort(bar, parity, abort_flag, where);
       return bar_and(HANDOFF_BAR, 64, w);
@@ -228,7 +242,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int i = -2; i < n_qt; ++i) {
         if (i >= 0) {
           if (!handoff(&p_full[i & 1], (i >> 1) & 1, 54)) break;
-          if (!handoff(ds_full, i & 1, 55)) break;
+          if (i + 1 < n_qt && !handoff(dp_free, i & 1, 56)) break;
+          if (!handoff(ds_full(i), (i >> 1) & 1, 55)) break;
         }
         if (i + 2 < n_qt && !handoff(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, 53)) break;
       }
@@ -272,7 +287,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // One loop issues everything, the first steps included, so that every MMA
     // group exists once in the binary: code run once per CTA falls out of the
     // instruction cache between CTAs and then issues several times slower.
-    // Iteration i: dV(i), dK(i) (i >= 0); dP(i+1) (0 <= i+1 < n); S(i+2) (i+2 < n).
+    // Iteration i: dV(i) (i >= 0); dP(i+1) (0 <= i+1 < n); dK(i) (i >= 0); S(i+2) (i+2 < n).
 #ifdef LAGA_TRACE
     // trace build only: cycles spent at each hand-off
     long long st_cyc[3] = {0, 0, 0};
@@ -295,18 +310,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma4_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), pt + packed_col(2), pt + packed_col(3),
                      do_mn, do_mn + (2048 >> 4), do_mn + (4096 >> 4), do_mn + (6144 >> 4), IDESC_DV,
                      i > 0 ? 1u : 0u);
+        if (i + 1 < n_qt) {
+          if (!ready()) { ok = false; break; }  // dP^T(i) read out: dP(i+1) may overwrite it
+          issue_dp(i + 1);
+        }
         DKDV_STAT_BEGIN(1)
         if (!ready()) { ok = false; break; }  // dS^T(i)
         DKDV_STAT_END(1)
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, i);
-        // dK += dS^T Q_i : all 192 head dims in one product
+        // dK += dS^T Q_i : all 192 head dims in one product; dS^T(i) sits in S^T(i)'s buffer
         const uint64_t q_mn = stage_desc(i, 0, QBOX);
-        const uint32_t ds = tmem + COL_DP;
-        mma4_ts_warp(tmem + COL_DK, ds + packed_col(0), ds + packed_col(1), ds + packed_col(2), ds + packed_col(3),
-                     q_mn, q_mn + (2048 >> 4), q_mn + (4096 >> 4), q_mn + (6144 >> 4), IDESC_DK, i > 0 ? 1u : 0u);
+        mma4_ts_warp(tmem + COL_DK, pt + packed_col_ds(0), pt + packed_col_ds(1), pt + packed_col_ds(2),
+                     pt + packed_col_ds(3), q_mn, q_mn + (2048 >> 4), q_mn + (4096 >> 4), q_mn + (6144 >> 4),
+                     IDESC_DK, i > 0 ? 1u : 0u);
         mma_commit_warp(&q_empty[i % NSTAGE]);
+      } else if (i + 1 == 0 && n_qt > 0) {
+        issue_dp(0);  // its stage was handed over before S(0)
       }
-      if (i + 1 >= 0 && i + 1 < n_qt) issue_dp(i + 1);  // its stage was handed over before S(i+1)
       if (i + 2 < n_qt) {
         DKDV_STAT_BEGIN(2)
         if (!ready()) { ok = false; break; }  // Q_{i+2}, dO_{i+2}, lse and D rows
@@ -414,17 +434,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t u[32];
         tmem_ld32(dp_addr + 32 * half, u);
         tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dp_free);  // dP(i+1) may overwrite the dP^T columns
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           w[k] = pack_bf16x2(pr[2 * k] * (__uint_as_float(u[2 * k]) - dlt[2 * k]),
                              pr[2 * k + 1] * (__uint_as_float(u[2 * k + 1]) - dlt[2 * k + 1]));
-        tmem_st16(dp_addr + 32 * half, w);
+        // dS^T packed over this half's second 16 score columns of S^T(i) (already read)
+        tmem_st16(s_addr + 32 * half + 16, w);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(ds_full(i));
       if (lane == 0) LAGA_TRACE_POINT(dkdv, 13, i);
     }
     if (ok && warp_wait(acc_done, 0, 64)) {

@@ -10,13 +10,16 @@
 // The RoPE-key concat is folded in as in the forward: S = Q_nope K_nope^T +
 // Q_rope k_rope^T, and dq's last 64 columns come from the k_rope tile.
 //
-// TMEM columns: S [0,128), dP/dS [128,256), dq [256,448), dO [448,512).
-// S and dP have one buffer each. The softmax warps copy S(j) to registers and
-// release it at once, so S(j+1) is computed while they work on tile j; dS(j)
-// is written as packed bf16 over dP(j) and read from there by dq(j); dP(j+1)
-// follows dq(j) in the MMA order. The loop-carried chain per key tile is then
-// the dS half of the softmax plus dq(j) and dP(j+1); S(j+1) and the
-// exponentials of tile j+1 run beside it.
+// TMEM columns: two step buffers [0,128) and [128,256), dq [256,448), dO
+// [448,512). Step j uses buffer j % 2 for all three of its tiles in turn: S(j),
+// which the softmax warps copy to registers and release at once; then dP(j);
+// then dS(j), packed as bf16 over the dP(j) columns each warpgroup has read,
+// from where dq(j) reads it. MMA order S(0) S(1)? dP(0) | dq(j) dP(j+1) S(j+2) |
+// ...: dP(j+1) needs only S(j+1) released, not dq(j) done, so the loop-carried
+// chain is the tensor work itself (dq 768 + dP 512 + S 768 cycles per 128-key
+// step) with the softmax beside it. Measured on GB300 with one S and one dP/dS
+// buffer (dP(j+1) after dq(j)): 2425 cycles per step, the softmax's dS half and
+// dq(j) + dP(j+1) in one chain.
 //
 // Warp roles (352 threads):
 //   warp 0      lane 0: TMA for Q once, then key tiles
@@ -48,7 +51,9 @@ constexpr int OFF_V = OFF_K + K_STAGES * K_BYTES;
 constexpr int OFF_BARS = OFF_V + V_STAGES * V_BYTES;
 constexpr int SMEM_BYTES = OFF_BARS + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DO = 448;
+constexpr uint32_t COL_DQ = 256, COL_DO = 448;
+// the TMEM buffer of step j (S(j), then dP(j), then dS(j))
+__device__ __forceinline__ uint32_t step_buf(int j) { return static_cast<uint32_t>(j & 1) * 128u; }
 constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_DQ = idesc_bf16(128, 192, false, true);
 constexpr int NTHREADS = 352;
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* v_full = bars + 7;   // [V_STAGES]
   uint64_t* v_empty = bars + 8;  // [V_STAGES]
   uint64_t* s_full = bars + 9;   // S(j) in TMEM
-  uint64_t* s_free = bars + 10;  // S(j) copied out by every softmax warp
+  uint64_t* s_free = bars + 10;  // S(j) copied out by every softmax warp: dP(j) may overwrite it
   uint64_t* dp_full = bars + 11; // dP(j) in TMEM
   uint64_t* ds_full = bars + 12; // dS(j) packed over dP(j)
   uint64_t* dq_done = bars + 13;
@@ -189,10 +194,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // The whole warp runs the issue loop; an elected lane issues. One loop issues
     // everything (code run once per CTA falls out of the instruction cache between
-    // CTAs and then issues several times slower). Iteration j: S(j+1) once S(j)
-    // is released, dq(j) once dS(j) is in, then dP(j+1). Each barrier is tested
-    // (without blocking) inside the MMA group that precedes its use, before that
-    // group's last block of four, and consumed as a token after the group.
+    // CTAs and then issues several times slower). Iteration j: dq(j) once dS(j) is
+    // in; dP(j+1) once S(j+1) is released; S(j+2) into the buffer dq(j) has just
+    // read. Each barrier is tested (without blocking) inside the MMA group that
+    // precedes its use, before that group's last block of four, and consumed as a
+    // token after the group.
     bool ok = warp_wait_or_abort(q_full, 0, abort_flag, 73) && warp_wait_or_abort(do_tmem, 0, abort_flag, 77);
     bool issued = false;
     tc_fence_after();
@@ -204,12 +210,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int c = 0; c < 3; ++c) {  // head dims [64c, 64c + 64): four K16 steps in box c (one elect each)
         if (c == 2) tests();
         const uint32_t o = (c * BOX) >> 4;
-        mma4_ss_warp(tmem + COL_S, q_desc + o, q_desc + o + 2, q_desc + o + 4, q_desc + o + 6, k_desc + o,
+        mma4_ss_warp(tmem + step_buf(j), q_desc + o, q_desc + o + 2, q_desc + o + 4, q_desc + o + 6, k_desc + o,
                      k_desc + o + 2, k_desc + o + 4, k_desc + o + 6, IDESC_S, c > 0 ? 1u : 0u);
       }
       mma_commit_warp(s_full);
     };
-    auto issue_dp = [&](int j, auto&& tests) {  // dP(j) = dO V_j^T
+    auto issue_dp = [&](int j, auto&& tests) {  // dP(j) = dO V_j^T, over S(j)'s columns
       const int s = j % V_STAGES;
       const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V + s * V_BYTES), 16, 1024);
 #pragma unroll
@@ -217,34 +223,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (c == 1) tests();
         const uint32_t a = tmem + COL_DO + 32 * c;
         const uint64_t v = v_desc + ((c * BOX) >> 4);
-        mma4_ts_warp(tmem + COL_DP, a, a + 8, a + 16, a + 24, v, v + 2, v + 4, v + 6, IDESC_S, c > 0 ? 1u : 0u);
+        mma4_ts_warp(tmem + step_buf(j), a, a + 8, a + 16, a + 24, v, v + 2, v + 4, v + 6, IDESC_S,
+                     c > 0 ? 1u : 0u);
       }
       mma_commit_warp(dp_full);
       mma_commit_warp(&v_empty[s]);
     };
     uint32_t tk = 0, tv = 0, tf = 0, td = 0;
-    for (int j = -1; j < n_kv && ok; ++j) {
-      const int jn = j + 1;
-      if (jn < n_kv) {  // S(j+1): needs K(j+1) and S(j) released
-        if (j >= 0 && !warp_wait_token(s_free, j & 1, tf, abort_flag, 78)) { ok = false; break; }
-        if (!warp_wait_token(&k_full[jn % K_STAGES], (jn / K_STAGES) & 1, tk, abort_flag, 74)) { ok = false; break; }
-        tc_fence_after();
-        issue_s(jn, [&]() {
-          if (j >= 0) td = mbar_test(ds_full, j & 1);
-        });
-        issued = true;
-      } else if (j >= 0) {
-        td = mbar_test(ds_full, j & 1);
-      }
+    for (int j = -2; j < n_kv && ok; ++j) {
+      const int j1 = j + 1, j2 = j + 2;
       if (j >= 0) {  // dq(j) += dS(j) K_j : A = dS (TMEM, packed bf16), B = key tile MN-major (N = 192)
         if (!warp_wait_token(ds_full, j & 1, td, abort_flag, 76)) { ok = false; break; }
         tc_fence_after();
         const int s = j % K_STAGES;
         const uint64_t k_mn = sdesc_sw128(smem_u32(smem + OFF_K + s * K_BYTES), BOX, 1024);
-        const uint32_t ds = tmem + COL_DP;
+        const uint32_t ds = tmem + step_buf(j);
 #pragma unroll
         for (int g = 0; g < BKV / 64; ++g) {  // keys [64g, 64g + 64)
-          if (g == BKV / 64 - 1 && jn < n_kv) tv = mbar_test(&v_full[jn % V_STAGES], (jn / V_STAGES) & 1);
+          if (g == BKV / 64 - 1 && j1 < n_kv) {
+            tf = mbar_test(s_free, j1 & 1);
+            tv = mbar_test(&v_full[j1 % V_STAGES], (j1 / V_STAGES) & 1);
+          }
           const int k = 4 * g;
           mma4_ts_warp(tmem + COL_DQ, ds + packed_col(k), ds + packed_col(k + 1), ds + packed_col(k + 2),
                        ds + packed_col(k + 3), k_mn + ((k * 2048) >> 4), k_mn + (((k + 1) * 2048) >> 4),
@@ -253,15 +252,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_commit_warp(&k_empty[s]);
       }
-      if (jn < n_kv) {  // dP(j+1): follows dq(j), which reads dS(j) from the same columns
-        if (!warp_wait_token(&v_full[jn % V_STAGES], (jn / V_STAGES) & 1, tv, abort_flag, 75)) { ok = false; break; }
+      if (j1 >= 0 && j1 < n_kv) {  // dP(j+1): S(j+1) released, V(j+1) in
+        if (!warp_wait_token(s_free, j1 & 1, tf, abort_flag, 78)) { ok = false; break; }
+        if (!warp_wait_token(&v_full[j1 % V_STAGES], (j1 / V_STAGES) & 1, tv, abort_flag, 75)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        issue_dp(jn, [&]() {
-          if (jn + 1 < n_kv) {
-            tf = mbar_test(s_free, jn & 1);
-            tk = mbar_test(&k_full[(jn + 1) % K_STAGES], ((jn + 1) / K_STAGES) & 1);
-          }
+        issue_dp(j1, [&]() {
+          if (j2 < n_kv) tk = mbar_test(&k_full[j2 % K_STAGES], (j2 / K_STAGES) & 1);
         });
+        issued = true;
+      }
+      if (j2 < n_kv) {  // S(j+2): K(j+2) in; its buffer was last read by dq(j), issued above
+        if (!warp_wait_token(&k_full[j2 % K_STAGES], (j2 / K_STAGES) & 1, tk, abort_flag, 74)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(j2, [&]() {
+          if (j1 >= 0 && j1 < n_kv) td = mbar_test(ds_full, j1 & 1);
+        });
+        issued = true;
+      } else if (j1 >= 0 && j1 < n_kv) {
+        td = mbar_test(ds_full, j1 & 1);
       }
     }
     if (ok) {
@@ -318,12 +332,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) LAGA_TRACE_POINT(dq, 10, j);
       tc_fence_after();
       uint32_t x[64];
-      tmem_ld32(tmem + COL_S + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
-      tmem_ld32(tmem + COL_S + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+      const uint32_t buf = tmem + step_buf(j) + lane_off + 64 * half;
+      tmem_ld32(buf, *reinterpret_cast<uint32_t(*)[32]>(x));
+      tmem_ld32(buf + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);  // S(j+1) may now overwrite S(j)
+      if (lane == 0) mbar_arrive(s_free);  // dP(j) may now overwrite S(j)
       const int kv_first = j * BKV + 64 * half;  // this thread's first key column
       float pr[64];
       if (kv_first + 63 <= limit) {  // every key of the half-tile visible
@@ -336,9 +351,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (!warp_wait(dp_full, ph, 83)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t dp_addr = tmem + COL_DP + lane_off + 64 * half;
-      tmem_ld32(dp_addr, *reinterpret_cast<uint32_t(*)[32]>(x));
-      tmem_ld32(dp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+      tmem_ld32(buf, *reinterpret_cast<uint32_t(*)[32]>(x));
+      tmem_ld32(buf + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
       tmem_wait_ld();
       uint32_t w[32];
 #pragma unroll
@@ -346,7 +360,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         w[k] = pack_bf16x2(pr[2 * k] * (__uint_as_float(x[2 * k]) - Drow),
                            pr[2 * k + 1] * (__uint_as_float(x[2 * k + 1]) - Drow));
       // dS packed into the first 32 of this warpgroup's own 64 dP columns
-      tmem_st32(dp_addr, w);
+      tmem_st32(buf, w);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

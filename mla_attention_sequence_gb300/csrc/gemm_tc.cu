@@ -9,7 +9,8 @@
 // One persistent kernel template serves all three. Warp roles (224 threads):
 //   warp 0      TMA producer of the A tiles into a STAGES-deep shared-memory ring
 //   warp 1      TMEM allocator; the whole warp runs the MMA issue loop
-//   warps 2..5  epilogue: TMEM -> registers -> bf16 -> global
+//   warps 2..5  epilogue: TMEM -> registers -> bf16 -> shared memory -> tensor-map
+//               store, per warp in [32 rows][32 cols] boxes through two buffers
 //   warp 6      TMA producer of the B tiles
 // Two TMEM accumulators let the epilogue of one tile overlap the next tile's
 // main loop. Operand tiles use the 128-byte swizzle; a K-major tile is
@@ -68,7 +69,10 @@ struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  // epilogue staging: 4 warps x 2 buffers x [32 rows][32 bf16] (64-byte swizzle)
+  static constexpr int EPI_BOX = 32 * 64;
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr bool A_MN = (MODE == DW);
   static constexpr bool B_MN = (MODE != DCKV);
@@ -81,6 +85,7 @@ template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(224, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+                   const __grid_constant__ CUtensorMap mapO0, const __grid_constant__ CUtensorMap mapO1,
                    const GemmParams p) {
   using C = Cfg<MODE, BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -88,7 +93,8 @@ __global__ void __launch_bounds__(224, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t* sEpi = smem + STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + C::EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;
@@ -249,9 +255,23 @@ __global__ void __launch_bounds__(224, 1)
     }
   } else {
     // Epilogue warps 2..5: warp (w % 4) may read TMEM lanes 32*(w%4) .. +31.
+    // Each warp writes its 32 rows of a tile as [32 rows][32 cols] boxes: a
+    // 32-column chunk goes TMEM -> registers -> bf16 -> one of the warp's two
+    // shared-memory buffers (64-byte swizzle) -> a tensor-map store issued by lane
+    // 0. Measured on GB300: row-per-thread 16-byte global stores from all SMs at
+    // once run at ~64 cycles per warp instruction, coalesced ones at ~24; the
+    // K/V rebuild writes 1 GB, so its epilogue set the pace with direct stores.
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    uint8_t* ebuf = sEpi + (warp - 2) * 2 * C::EPI_BOX;
+    const CUtensorMap* map0 = &mapO0;
+    const CUtensorMap* map1 = &mapO1;
+    if (lane == 0) {
+      tma_prefetch_desc(map0);
+      tma_prefetch_desc(map1);
+    }
     int local = 0;
+    int chunk = 0;  // chunks stored by this warp so far (buffer = chunk & 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -262,43 +282,50 @@ __global__ void __launch_bounds__(224, 1)
       tc_fence_after();
       int b, m, n;
       tile_coords(p, tile, b, m, n);
-      bf16* out;
+      const CUtensorMap* omap;
       int n0;
       if constexpr (MODE == DCKV) {
-        out = p.out0;
+        omap = map0;
         n0 = n * BN;
       } else {
         const bool second = n >= p.n_tiles_first;
-        out = second ? p.out1 : p.out0;
+        omap = second ? map1 : map0;
         n0 = (second ? n - p.n_tiles_first : n) * BN;
       }
-      const int row = m * BM + row_in_tile;
-      const bool valid = row < p.rows_valid;
-      bf16* orow = out + static_cast<long long>(b) * p.out_batch_stride + static_cast<long long>(row) * p.ldo + n0;
+      const int y0 = m * BM + quarter * 32;  // first row of this warp's boxes
       const uint32_t t_row = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
         uint32_t r[32];
         tmem_ld32(t_row + c0, r);
         tmem_wait_ld();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        if (c0 + 32 == BN) {  // the accumulator has been read out: the MMA may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        uint8_t* box = ebuf + (chunk & 1) * C::EPI_BOX;
+        if (lane == 0) bulk_wait_read_1();  // the store that last read this buffer is done reading
+        __syncwarp();
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-            dst[v] = w;
-          }
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+          w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+          w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+          w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+          *reinterpret_cast<uint4*>(box + sw64_offset(lane, v)) = w;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(omap, box, n0 + c0, y0, b);
+          bulk_commit_group();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
       if (MODE == RECON_FWD && lane == 0 && local < 512) LAGA_TRACE_POINT(gemm, 10, local);
     }
+    if (lane == 0) bulk_wait_read_all();  // shared memory must not go away under a store
   }
 
   tc_fence_before();
@@ -312,7 +339,8 @@ __global__ void __launch_bounds__(224, 1)
 
 template <int MODE, int BN, int STAGES>
 LaunchResult launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                         const CUtensorMap& b1, const GemmParams& p, cudaStream_t st) {
+                         const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1, const GemmParams& p,
+                         cudaStream_t st) {
   using C = Cfg<MODE, BN, STAGES>;
   LaunchResult r;
   auto kern = gemm_tc_kernel<MODE, BN, STAGES>;
@@ -326,7 +354,7 @@ LaunchResult launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUt
   const int grid = std::min(tiles, sm_count());
   GemmParams pp = p;
   pp.status = device_status_ptr();
-  kern<<<grid, 224, C::SMEM, st>>>(a0, a1, b0, b1, pp);
+  kern<<<grid, 224, C::SMEM, st>>>(a0, a1, b0, b1, o0, o1, pp);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "gemm_tc_kernel launch";
   return r;
@@ -339,6 +367,16 @@ CUresult tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
   const uint32_t box[2] = {box_inner, box_outer};
   return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output map of the epilogue's [32 rows][32 cols] bf16 boxes (64-byte swizzle)
+// over a [batches][rows][cols] tensor; rows beyond `rows` are clipped.
+CUresult tmap_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t batches,
+                  uint64_t batch_stride_elems) {
+  const uint64_t dims[3] = {cols, rows, batches};
+  const uint64_t strides[2] = {cols * 2, batch_stride_elems * 2};
+  const uint32_t box[3] = {32, 32, 1};
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace
@@ -381,8 +419,18 @@ LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, con
   p.ldo = static_cast<long long>(N);
   p.out_batch_stride = static_cast<long long>(rows_pad) * N;
   p.rows_valid = rows_pad;
-  if (BN == 256) return launch_gemm<RECON_FWD, 256, 4>(a0, a0, b0, b1, p, st);
-  return launch_gemm<RECON_FWD, 128, 6>(a0, a0, b0, b1, p, st);
+  CUtensorMap o0, o1;
+  r.cu = tmap_out(&o0, k_ws, N, static_cast<uint64_t>(rows_pad), static_cast<uint64_t>(d.B),
+                  static_cast<uint64_t>(rows_pad) * N);
+  if (r.cu == CUDA_SUCCESS)
+    r.cu = tmap_out(&o1, v_ws, N, static_cast<uint64_t>(rows_pad), static_cast<uint64_t>(d.B),
+                    static_cast<uint64_t>(rows_pad) * N);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor map K/V out";
+    return r;
+  }
+  if (BN == 256) return launch_gemm<RECON_FWD, 256, 4>(a0, a0, b0, b1, o0, o1, p, st);
+  return launch_gemm<RECON_FWD, 128, 6>(a0, a0, b0, b1, o0, o1, p, st);
 }
 
 LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws, const bf16* W_UK,
@@ -416,8 +464,15 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
   p.ldo = d.d_c;
   p.out_batch_stride = static_cast<long long>(d.S) * d.d_c;
   p.rows_valid = d.S;
-  if (BN == 256) return launch_gemm<DCKV, 256, 4>(a0, a1, b0, b1, p, st);
-  return launch_gemm<DCKV, 128, 6>(a0, a1, b0, b1, p, st);
+  CUtensorMap o0;
+  r.cu = tmap_out(&o0, dc_kv, static_cast<uint64_t>(d.d_c), static_cast<uint64_t>(d.S), static_cast<uint64_t>(d.B),
+                  static_cast<uint64_t>(d.S) * d.d_c);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor map dc_kv out";
+    return r;
+  }
+  if (BN == 256) return launch_gemm<DCKV, 256, 4>(a0, a1, b0, b1, o0, o0, p, st);
+  return launch_gemm<DCKV, 128, 6>(a0, a1, b0, b1, o0, o0, p, st);
 }
 
 LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws, const bf16* dv_ws, bf16* dW_UK,
@@ -449,8 +504,15 @@ LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws,
   p.ldo = static_cast<long long>(N);
   p.out_batch_stride = 0;
   p.rows_valid = d.d_c;
-  if (BN == 256) return launch_gemm<DW, 256, 4>(a0, a0, b0, b1, p, st);
-  return launch_gemm<DW, 128, 6>(a0, a0, b0, b1, p, st);
+  CUtensorMap o0, o1;
+  r.cu = tmap_out(&o0, dW_UK, N, static_cast<uint64_t>(d.d_c), 1, static_cast<uint64_t>(d.d_c) * N);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_out(&o1, dW_UV, N, static_cast<uint64_t>(d.d_c), 1, static_cast<uint64_t>(d.d_c) * N);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor map dW out";
+    return r;
+  }
+  if (BN == 256) return launch_gemm<DW, 256, 4>(a0, a0, b0, b1, o0, o1, p, st);
+  return launch_gemm<DW, 128, 6>(a0, a0, b0, b1, o0, o1, p, st);
 }
 
 }  // namespace laga
