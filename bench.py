@@ -611,11 +611,12 @@ def run_variant_sweep(args):
 
 
 # ---------------------------------------------------------------- eager (unfused) baseline
-def eager_forward_backward(t: dict, p: Problem, scale: float):
+def eager_forward_backward(t: dict, p: Problem, scale: float, saved: dict | None = None):
     """The attention block written as separate library operations, the 'eager'
     setting: reconstruction matmuls, the RoPE-key concat, QK^T, mask, softmax in
     fp32, PV, each a separate cuBLAS / PyTorch kernel with its intermediates in
-    HBM, and torch autograd for the backward. bf16 matmuls with fp32 softmax."""
+    HBM, and torch autograd for the backward. bf16 matmuls with fp32 softmax.
+    `saved` (if given) receives the memory autograd holds after the forward."""
     import torch
     B, Sq, n_h, S = p.B, p.Sq, p.n_h, p.skv_eff
     q = t["q"].detach().requires_grad_()
@@ -623,6 +624,7 @@ def eager_forward_backward(t: dict, p: Problem, scale: float):
     kr = t["k_rope"].detach().requires_grad_()
     wk = t["W_UK"].detach().requires_grad_()
     wv = t["W_UV"].detach().requires_grad_()
+    base = torch.cuda.memory_allocated(q.device)
     k_nope = (c[:, :S] @ wk).view(B, S, n_h, p.d_nope)
     v = (c[:, :S] @ wv).view(B, S, n_h, p.d_v)
     k = torch.cat([k_nope, kr[:, :S, None, :].expand(B, S, n_h, p.d_rope)], dim=-1)
@@ -635,9 +637,158 @@ def eager_forward_backward(t: dict, p: Problem, scale: float):
         lse = torch.logsumexp(sc, dim=-1)
     prob = torch.softmax(sc, dim=-1).to(torch.bfloat16)
     out = torch.matmul(prob, v.permute(0, 2, 1, 3)).permute(0, 2, 1, 3)
+    if saved is not None:
+        torch.cuda.synchronize()
+        saved["bytes"] = torch.cuda.memory_allocated(q.device) - base
     out.backward(t["dout"])
     return out.detach(), lse.detach(), {"dq": q.grad, "dc_kv": c.grad, "dk_rope": kr.grad, "dW_UK": wk.grad,
                                         "dW_UV": wv.grad}
+
+
+def eager_absorbed_forward_backward(t: dict, p: Problem, scale: float, saved: dict | None = None):
+    """The absorbed MLA form as separate library operations (the eager setting):
+    q_lat = q_nope W_UK^T per head, scores against [c_kv | k_rope], softmax in fp32,
+    attention over the latent, output through W_UV, torch autograd backward.
+    `saved` (if given) receives the memory autograd holds after the forward."""
+    import torch
+    B, Sq, n_h, S = p.B, p.Sq, p.n_h, p.skv_eff
+    q = t["q"].detach().requires_grad_()
+    c = t["c_kv"].detach().requires_grad_()
+    kr = t["k_rope"].detach().requires_grad_()
+    wk = t["W_UK"].detach().requires_grad_()
+    wv = t["W_UV"].detach().requires_grad_()
+    base = torch.cuda.memory_allocated(q.device)
+    q_lat = torch.einsum("bihd,chd->bihc", q[..., :p.d_nope], wk.view(p.d_c, n_h, p.d_nope))
+    q_abs = torch.cat([q_lat, q[..., p.d_nope:]], dim=-1)  # [B, Sq, n_h, d_c + d_rope]
+    key = torch.cat([c[:, :S], kr[:, :S]], dim=-1)  # one key for every head
+    sc = torch.einsum("bihc,bjc->bhij", q_abs, key).float() * scale
+    if p.causal:
+        pos = torch.arange(Sq, device=q.device) + p.q_offset
+        sc = sc.masked_fill(torch.arange(S, device=q.device)[None, :] > pos[:, None], float("-inf"))
+    prob = torch.softmax(sc, dim=-1).to(torch.bfloat16)
+    ctx = torch.einsum("bhij,bjc->bihc", prob, c[:, :S])
+    out = torch.einsum("bihc,chd->bihd", ctx, wv.view(p.d_c, n_h, p.d_v))
+    if saved is not None:
+        torch.cuda.synchronize()
+        saved["bytes"] = torch.cuda.memory_allocated(q.device) - base
+    out.backward(t["dout"])
+    return out.detach(), {"dq": q.grad, "dc_kv": c.grad, "dk_rope": kr.grad, "dW_UK": wk.grad, "dW_UV": wv.grad}
+
+
+def run_memory_sweep(args):
+    """Device memory of one training step (forward + backward) of the attention
+    block, per implementation, over the last-rank SP=8 shards of seq in
+    {4096, 8192, 16384} x n_h in {32, 64, 128}: the bytes kept from the forward for
+    the backward ('saved': autograd's holdings for the eager forms; the outputs
+    and the kept workspace for the library's) and the step's peak above the
+    inputs ('peak'). One JSON line per shape, then a fit of the absorbed-minus-LAGA
+    gap against seq x n_h."""
+    import torch
+
+    from mla_attention_sequence_gb300 import build as build_mod
+    from mla_attention_sequence_gb300 import laga
+    from mla_attention_sequence_gb300.configs import dsv3_rank
+
+    build_mod.build()
+    dev = torch.device("cuda", 0)
+    rows = []
+    for seq in (4096, 8192, 16384):
+        for n_h in (32, 64, 128):
+            p = dsv3_rank(7, seq=seq, n_h=n_h)
+            x = make_inputs(p, SEED)
+            t = {k: torch.from_numpy(v).to(dev).to(torch.bfloat16) for k, v in x.items()}
+            scale = 1.0 / float(np.sqrt(p.d_qk))
+            line = {"mode": "memory", "workload": p.name, "S": seq, "n_h": n_h, "Sq": p.Sq}
+            outs_bytes = (p.B * p.Sq * p.n_h * p.d_v * 2 + p.B * p.n_h * p.Sq * 4)
+
+            def measure(fn):
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
+                base = torch.cuda.memory_allocated(dev)
+                torch.cuda.reset_peak_memory_stats(dev)
+                info = fn() or {}
+                torch.cuda.synchronize()
+                info["peak"] = int(torch.cuda.max_memory_allocated(dev) - base)
+                return info
+
+            def laga_reuse():
+                buf = laga.alloc_step(p, t)
+                laga.step(buf)
+                # kept from the forward for the backward: the rebuilt K_nope / V (the
+                # forward's part of the shared workspace) and out, lse
+                return {"saved": int(laga.fwd_workspace_bytes(p)) + outs_bytes, "workspace": int(buf.ws.numel())}
+
+            def laga_rebuild():
+                ws_f = laga.fwd_workspace_bytes(p)
+                out, lse = laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True)
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()  # the forward's workspace is gone; K/V are rebuilt in the backward
+                laga.bwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], out, lse, t["dout"], p.q_offset, True)
+                return {"saved": outs_bytes, "fwd_workspace": int(ws_f), "bwd_workspace": int(laga.bwd_workspace_bytes(p))}
+
+            def absorbed():
+                nb = laga.absorbed_workspace_bytes(p)
+                ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+                laga.absorbed_fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True,
+                                  workspace=ws)
+                # the absorbed form's backward needs q_lat and ctx (the workspace) kept
+                return {"saved": int(nb) + outs_bytes, "workspace": int(nb), "note": "forward only on the GPU"}
+
+            def eager_expl():
+                saved = {}
+                r = eager_forward_backward(t, p, scale, saved)
+                del r
+                return {"saved": int(saved["bytes"])}
+
+            def eager_abs():
+                saved = {}
+                r = eager_absorbed_forward_backward(t, p, scale, saved)
+                del r
+                return {"saved": int(saved["bytes"])}
+
+            # forward times (median of 5, L2 flushed): the library's forward and the absorbed form's
+            flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+            stream = torch.cuda.current_stream(dev)
+            ws_l = torch.empty(laga.fwd_workspace_bytes(p), dtype=torch.uint8, device=dev)
+            ws_a = torch.empty(laga.absorbed_workspace_bytes(p), dtype=torch.uint8, device=dev)
+            f_l = lambda: laga.fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True,
+                                   workspace=ws_l)
+            f_a = lambda: laga.absorbed_fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True,
+                                            workspace=ws_a)
+            f_l(), f_a()
+            line["ms_fwd"] = {"laga": _time_events(f_l, 5, flush, stream), "absorbed": _time_events(f_a, 5, flush, stream)}
+            del flush, ws_l, ws_a
+            line["laga_reuse_kv"] = measure(laga_reuse)
+            line["laga_rebuild_kv"] = measure(laga_rebuild)
+            line["absorbed"] = measure(absorbed)
+            if not args.no_eager:
+                line["eager_explicit"] = measure(eager_expl)
+                line["eager_absorbed"] = measure(eager_abs)
+            print(json.dumps(line), flush=True)
+            rows.append(line)
+            del t
+            torch.cuda.empty_cache()
+    # the absorbed form's extra saved bytes against LAGA's (rebuild): linear in Sq x n_h?
+    xs = np.array([r["Sq"] * r["n_h"] for r in rows], dtype=float)
+    gap = np.array([r["absorbed"]["saved"] - r["laga_rebuild_kv"]["saved"] for r in rows], dtype=float)
+    A = np.vstack([xs, np.ones_like(xs)]).T
+    coef, res, _, _ = np.linalg.lstsq(A, gap, rcond=None)
+    pred = A @ coef
+    print(json.dumps({"mode": "memory_fit", "quantity": "absorbed saved - laga (rebuild) saved, bytes",
+                      "bytes_per_query_row_and_head": coef[0], "intercept": coef[1],
+                      "max_rel_residual": float(np.max(np.abs(pred - gap) / np.maximum(np.abs(gap), 1.0)))}),
+          flush=True)
+    if not args.no_eager:
+        # eager forms: the absorbed-minus-explicit gap per score element (query x key x head)
+        els = np.array([r["Sq"] * r["S"] * r["n_h"] for r in rows], dtype=float)
+        eg = np.array([r["eager_absorbed"]["saved"] - r["eager_explicit"]["saved"] for r in rows], dtype=float)
+        ratio = eg / els
+        print(json.dumps({"mode": "memory_fit", "quantity": "eager absorbed saved - eager explicit saved, bytes",
+                          "bytes_per_score_element": {"min": float(ratio.min()), "max": float(ratio.max())},
+                          "relative_gap_pct": [round(100 * (r["eager_absorbed"]["saved"] /
+                                                            r["eager_explicit"]["saved"] - 1), 2) for r in rows]}),
+              flush=True)
+    return 0
 
 
 def run_eager(args, name: str):
@@ -732,6 +883,9 @@ def main(argv=None):
                     help="time fwd+bwd (materialised K/V) and the forward of both K/V variants over the sweep "
                          "shapes instead")
     ap.add_argument("--sweep-filter", default="", help="only sweep shapes whose name contains this string")
+    ap.add_argument("--memory-sweep", action="store_true",
+                    help="device memory of one training step per implementation over the sweep shapes instead")
+    ap.add_argument("--no-eager", action="store_true", help="memory sweep without the eager (torch) forms")
     ap.add_argument("--eager", action="store_true",
                     help="time the unfused (eager) baseline beside the fused path on --workload instead")
     args = ap.parse_args(argv)
@@ -746,6 +900,8 @@ def main(argv=None):
         return run_variant_sweep(args)
     if args.eager:
         return run_eager(args, args.workload)
+    if args.memory_sweep:
+        return run_memory_sweep(args)
     if args.impl == "reference":
         p = GROUPS[args.workload][-1] if args.workload in GROUPS else NAMED[args.workload]
         return run_reference(args, p)

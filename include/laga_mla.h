@@ -194,6 +194,26 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
 laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
                                  const void* W_UV, void* k_nope, void* v, laga_stream_t stream);
 
+/* The absorbed MLA form, forward, for comparison with the library's own path.
+ * Source: the LAGA page's Abstract (weekinpapers, "A Training-Memory Regression
+ * in MLA Sequence Parallelism ..."): Megatron-Core's absorbed form folds W_UK
+ * into the query and attends over the compressed latent itself; LAGA keeps its
+ * latent-only communication but rejects the reformulation because of the
+ * memory its intermediates take. Per head h:
+ *   q_lat  = q_nope_h . W_UK_h^T                         [B, Sq, d_c]
+ *   s_ij   = softmax_scale * ([q_lat | q_rope]_i . [c_kv | k_rope]_j)  (masked as above)
+ *   ctx_i  = sum_j softmax_j(s_ij) c_kv_j                [B, Sq, d_c]
+ *   out_i  = ctx_i . W_UV_h
+ * The scores are the explicit form's, so out and lse equal laga_mla_fwd's up to
+ * rounding. The intermediates q_lat and ctx (n_h * d_c values per query row
+ * each) live in the workspace: laga_mla_absorbed_fwd_workspace_size bytes,
+ * 256-byte aligned. Supported: bf16 with the tensor-core dims, one query
+ * segment, variant AUTO. Arguments, layouts and errors as for laga_mla_fwd. */
+size_t laga_mla_absorbed_fwd_workspace_size(const laga_mla_desc* desc);
+laga_status laga_mla_absorbed_fwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
+                                  const void* W_UK, const void* W_UV, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, laga_stream_t stream);
+
 /* Largest workspace, in bytes, that laga_mla_fwd_noalloc can stand in for. */
 #define LAGA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -468,6 +468,44 @@ laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, co
   return from_launch(simt_reconstruct(d, bf, c_kv, W_UK, W_UV, k_nope, v, !bf, s));
 }
 
+size_t laga_mla_absorbed_fwd_workspace_size(const laga_mla_desc* desc) {
+  Dims d{};
+  laga_status st;
+  if (plan(desc, &d, &st, false) != Path::TensorCore || d.q_split > 0) return 0;
+  const size_t lat = align_up(static_cast<size_t>(d.B) * d.Sq * d.n_h * d.d_c * 2, 256);
+  return 2 * lat;  // q_lat and the latent-space context
+}
+
+laga_status laga_mla_absorbed_fwd(const laga_mla_desc* desc, const void* q, const void* c_kv, const void* k_rope,
+                                  const void* W_UK, const void* W_UV, void* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, laga_stream_t stream) {
+  Dims d{};
+  laga_status st;
+  const Path path = plan(desc, &d, &st, false);
+  if (path == Path::Invalid) return st;
+  if (path != Path::TensorCore || d.q_split > 0 || desc->variant != LAGA_VARIANT_AUTO)
+    return fail(LAGA_ERR_UNSUPPORTED,
+                "the absorbed form runs for bf16 with d_c=512, d_nope=d_v=128, d_rope=64, one query segment%s");
+  const void* ptrs[] = {q, c_kv, k_rope, W_UK, W_UV, out, lse};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return fail(LAGA_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned%s");
+  const size_t lat = align_up(static_cast<size_t>(d.B) * d.Sq * d.n_h * d.d_c * 2, 256);
+  if (!workspace || workspace_bytes < 2 * lat || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LAGA_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small%s");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  bf16* q_lat = static_cast<bf16*>(workspace);
+  bf16* ctx = reinterpret_cast<bf16*>(static_cast<char*>(workspace) + lat);
+  auto cb = [](const void* ptr) { return static_cast<const bf16*>(ptr); };
+  LaunchResult r = timed("absorbed_qlat_gemm", s, [&] { return tc_absorbed_qlat(d, cb(q), cb(W_UK), q_lat, s); });
+  if (r.ok())
+    r = timed("absorbed_attn", s,
+              [&] { return tc_absorbed_attn(d, q_lat, cb(q), cb(c_kv), cb(k_rope), ctx, lse, s); });
+  if (r.ok())
+    r = timed("absorbed_out_gemm", s,
+              [&] { return tc_absorbed_outproj(d, ctx, cb(W_UV), static_cast<bf16*>(out), s); });
+  return from_launch(r);
+}
+
 laga_status laga_mla_selftest_timeout(laga_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int* status = device_status_ptr();

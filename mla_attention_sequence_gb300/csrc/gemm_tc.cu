@@ -5,6 +5,8 @@
 //              (LAGA: per-head K/V rebuilt locally from the gathered latent)
 //   DCKV       dc_kv = dK_nope W_UK^T + dV W_UV^T          per batch element
 //   DW         dW_UK = sum_b c_kv[b]^T dK_nope[b], dW_UV likewise
+//   QLAT       q_lat_h = q_nope_h W_UK_h^T       per head (the absorbed form's query)
+//   OUTPROJ    out_h = ctx_h W_UV_h              per head (the absorbed form's output)
 //
 // One persistent kernel template serves all three. Warp roles (224 threads):
 //   warp 0      TMA producer of the A tiles into a STAGES-deep shared-memory ring
@@ -27,7 +29,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-enum Mode { RECON_FWD = 0, DCKV = 1, DW = 2 };
+enum Mode { RECON_FWD = 0, DCKV = 1, DW = 2, QLAT = 3, OUTPROJ = 4 };
 
 struct GemmParams {
   int* status;  // device status word (timeouts)
@@ -42,6 +44,9 @@ struct GemmParams {
   long long ldo;               // elements per output row
   long long out_batch_stride;  // elements between batch elements of the output
   int rows_valid;              // output rows (per batch element) that exist
+  int d_lat;                   // QLAT: latent width (output columns per head)
+  int a_head_stride;           // QLAT / OUTPROJ: A columns between heads
+  int b_head_stride;           // QLAT: B columns between heads
 };
 
 // Tile order: within a batch element, bands of GROUP_M m-tiles are walked n by n
@@ -75,7 +80,7 @@ struct Cfg {
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr bool A_MN = (MODE == DW);
-  static constexpr bool B_MN = (MODE != DCKV);
+  static constexpr bool B_MN = (MODE != DCKV && MODE != QLAT);
   static constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
   static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
   static_assert(BN % 64 == 0 && BN <= 256, "BN");
@@ -178,6 +183,23 @@ __global__ void __launch_bounds__(224, 1)
               tma_load_2d(a, second ? &mapA1 : &mapA0, &full[s], kk * BK, b * p.skv_pad + m * BM);
             else
               tma_load_2d(bsm, second ? &mapB1 : &mapB0, &full[s], kk * BK, n * BN);
+          } else if constexpr (MODE == QLAT) {
+            // tile n covers latent columns [n*BN, n*BN + BN) of head (n*BN) / d_c
+            const int h = (n * BN) / p.d_lat;
+            const int c0 = n * BN - h * p.d_lat;
+            if (load_a)
+              tma_load_2d(a, &mapA0, &full[s], h * p.a_head_stride + kb * BK, m * BM);
+            else
+              tma_load_2d(bsm, &mapB0, &full[s], h * p.b_head_stride + kb * BK, c0);
+          } else if constexpr (MODE == OUTPROJ) {
+            // tile n is head n (BN = the head's value width)
+            if (load_a) {
+              tma_load_2d(a, &mapA0, &full[s], n * p.a_head_stride + kb * BK, m * BM);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_2d(bsm + i * 8192, &mapB0, &full[s], n * BN + 64 * i, kb * BK);
+            }
           } else {
             const bool second = n >= p.n_tiles_first;
             const int n0 = (second ? n - p.n_tiles_first : n) * BN;
@@ -284,7 +306,7 @@ __global__ void __launch_bounds__(224, 1)
       tile_coords(p, tile, b, m, n);
       const CUtensorMap* omap;
       int n0;
-      if constexpr (MODE == DCKV) {
+      if constexpr (MODE == DCKV || MODE == QLAT || MODE == OUTPROJ) {
         omap = map0;
         n0 = n * BN;
       } else {
@@ -513,6 +535,58 @@ LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws,
   }
   if (BN == 256) return launch_gemm<DW, 256, 4>(a0, a0, b0, b1, o0, o1, p, st);
   return launch_gemm<DW, 128, 6>(a0, a0, b0, b1, o0, o1, p, st);
+}
+
+// ---- the absorbed MLA form's two projections (the rejected variant, run for comparison)
+
+LaunchResult tc_absorbed_qlat(const Dims& d, const bf16* q, const bf16* W_UK, bf16* q_lat, cudaStream_t st) {
+  LaunchResult r;
+  CUtensorMap a0, b0, o0;
+  const uint64_t rows = static_cast<uint64_t>(d.B) * d.Sq;
+  const uint64_t qcols = static_cast<uint64_t>(d.n_h) * (d.d_nope + d.d_rope);
+  const uint64_t lcols = static_cast<uint64_t>(d.n_h) * d.d_c;
+  r.cu = tmap_bf16_2d(&a0, q, qcols, rows, qcols * 2, 64, 128);
+  if (r.cu == CUDA_SUCCESS)
+    r.cu = tmap_bf16_2d(&b0, W_UK, static_cast<uint64_t>(d.n_h) * d.d_nope, d.d_c,
+                        static_cast<uint64_t>(d.n_h) * d.d_nope * 2, 64, 256);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_out(&o0, q_lat, lcols, rows, 1, rows * lcols);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor maps q_lat";
+    return r;
+  }
+  GemmParams p{};
+  p.m_tiles = static_cast<int>((rows + BM - 1) / BM);
+  p.n_tiles = static_cast<int>(lcols / 256);
+  p.n_tiles_first = p.n_tiles;
+  p.batches = 1;
+  p.k_blocks = d.d_nope / BK;
+  p.d_lat = d.d_c;
+  p.a_head_stride = d.d_nope + d.d_rope;
+  p.b_head_stride = d.d_nope;
+  return launch_gemm<QLAT, 256, 4>(a0, a0, b0, b0, o0, o0, p, st);
+}
+
+LaunchResult tc_absorbed_outproj(const Dims& d, const bf16* ctx, const bf16* W_UV, bf16* out, cudaStream_t st) {
+  LaunchResult r;
+  CUtensorMap a0, b0, o0;
+  const uint64_t rows = static_cast<uint64_t>(d.B) * d.Sq;
+  const uint64_t ccols = static_cast<uint64_t>(d.n_h) * d.d_c;
+  const uint64_t ocols = static_cast<uint64_t>(d.n_h) * d.d_v;
+  r.cu = tmap_bf16_2d(&a0, ctx, ccols, rows, ccols * 2, 64, 128);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b0, W_UV, ocols, d.d_c, ocols * 2, 64, 64);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_out(&o0, out, ocols, rows, 1, rows * ocols);
+  if (r.cu != CUDA_SUCCESS) {
+    r.what = "tensor maps absorbed output";
+    return r;
+  }
+  GemmParams p{};
+  p.m_tiles = static_cast<int>((rows + BM - 1) / BM);
+  p.n_tiles = d.n_h;
+  p.n_tiles_first = p.n_tiles;
+  p.batches = 1;
+  p.k_blocks = d.d_c / BK;
+  p.a_head_stride = d.d_c;
+  return launch_gemm<OUTPROJ, 128, 6>(a0, a0, b0, b0, o0, o0, p, st);
 }
 
 }  // namespace laga

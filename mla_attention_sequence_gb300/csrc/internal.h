@@ -103,6 +103,15 @@ LaunchResult tc_attn_bwd_dq(const Dims& d, const bf16* q, const bf16* k_rope, co
 // dk_rope = sum over heads of the per-head RoPE-key gradients.
 LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dk_rope, cudaStream_t st);
 
+// ---- the absorbed MLA form (for comparison; bf16, the tensor-core dims).
+// q_lat [B*Sq][n_h*d_c] = per head q_nope_h W_UK_h^T
+LaunchResult tc_absorbed_qlat(const Dims& d, const bf16* q, const bf16* W_UK, bf16* q_lat, cudaStream_t st);
+// ctx [B*Sq][n_h*d_c] (attention in latent space) and lse, from q_lat, q's RoPE part, c_kv, k_rope
+LaunchResult tc_absorbed_attn(const Dims& d, const bf16* q_lat, const bf16* q, const bf16* c_kv, const bf16* k_rope,
+                              bf16* ctx, float* lse, cudaStream_t st);
+// out [B*Sq][n_h*d_v] = per head ctx_h W_UV_h
+LaunchResult tc_absorbed_outproj(const Dims& d, const bf16* ctx, const bf16* W_UV, bf16* out, cudaStream_t st);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace laga

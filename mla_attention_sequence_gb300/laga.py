@@ -26,7 +26,8 @@ FLAG_REUSE_KV = 1
 
 EXPORTS = ("laga_mla_fwd_workspace_size", "laga_mla_bwd_workspace_size", "laga_mla_fwd", "laga_mla_bwd",
            "laga_mla_reconstruct", "laga_mla_check", "laga_status_string", "laga_mla_last_error",
-           "laga_mla_version", "laga_mla_selftest_timeout")
+           "laga_mla_version", "laga_mla_selftest_timeout", "laga_mla_absorbed_fwd",
+           "laga_mla_absorbed_fwd_workspace_size")
 
 
 class LagaDesc(ctypes.Structure):
@@ -66,6 +67,10 @@ def lib() -> ctypes.CDLL:
     L.laga_mla_fwd.restype = st
     L.laga_mla_bwd.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.laga_mla_bwd.restype = st
+    L.laga_mla_absorbed_fwd_workspace_size.argtypes = [pd]
+    L.laga_mla_absorbed_fwd_workspace_size.restype = sz
+    L.laga_mla_absorbed_fwd.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.laga_mla_absorbed_fwd.restype = st
     L.laga_mla_reconstruct.argtypes = [pd, vp, vp, vp, vp, vp, vp]
     L.laga_mla_reconstruct.restype = st
     L.laga_mla_check.argtypes = [vp]
@@ -197,6 +202,34 @@ def bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, q_offset: int = 0, causal: 
                              _ptr(out), _ptr(lse), _ptr(dout), _ptr(g["dq"]), _ptr(g["dc_kv"]), _ptr(g["dk_rope"]),
                              _ptr(g["dW_UK"]), _ptr(g["dW_UV"]), _ptr(ws), nbytes, _stream(dev)))
     return g
+
+
+def absorbed_fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset: int = 0, causal: bool = True,
+                 softmax_scale: float | None = None, workspace: torch.Tensor | None = None, out=None, lse=None):
+    """laga_mla_absorbed_fwd (the absorbed MLA form, for comparison): returns
+    (out [B,Sq,n_h,d_v], lse [B,n_h,Sq] fp32). The workspace holds the form's
+    intermediates q_lat and ctx ([B,Sq,n_h,d_c] each)."""
+    p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal)
+    d = make_desc(p, softmax_scale)
+    L = lib()
+    dev = q.device
+    if out is None:
+        out = torch.empty((p.B, p.Sq, p.n_h, p.d_v), dtype=q.dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((p.B, p.n_h, p.Sq), dtype=torch.float32, device=dev)
+    nbytes = int(L.laga_mla_absorbed_fwd_workspace_size(ctypes.byref(d)))
+    if nbytes == 0:
+        _raise_if(L.laga_mla_absorbed_fwd(ctypes.byref(d), None, None, None, None, None, None, None, None, 0,
+                                          _stream(dev)))
+    ws = _workspace(nbytes, dev, workspace)
+    _raise_if(L.laga_mla_absorbed_fwd(ctypes.byref(d), _ptr(q), _ptr(c_kv), _ptr(k_rope), _ptr(W_UK), _ptr(W_UV),
+                                      _ptr(out), _ptr(lse), _ptr(ws), nbytes, _stream(dev)))
+    return out, lse
+
+
+def absorbed_workspace_bytes(p: Problem) -> int:
+    d = make_desc(p)
+    return int(lib().laga_mla_absorbed_fwd_workspace_size(ctypes.byref(d)))
 
 
 def reconstruct(c_kv, W_UK, W_UV, n_h: int, variant: str = "auto"):

@@ -33,9 +33,14 @@ and dW sums over them.
 Everything is float64; inputs are upcast exactly. Row chunks only bound
 memory, they do not change the arithmetic.
 
+absorbed_forward writes out the absorbed MLA form the Abstract contrasts LAGA
+with (W_UK folded into the query, attention in the latent space); it reaches
+the same out and lse by a different factorisation of the same scores.
+
 Every function here has a pin in the CPU test suite (brute-force attention,
-the absorbed form, sequence-parallel shard consistency, finite differences,
-closed-form special cases and gradient identities).
+the absorbed form against the explicit one, sequence-parallel shard
+consistency, finite differences, closed-form special cases, hand-worked
+examples and gradient identities).
 """
 from __future__ import annotations
 
@@ -229,6 +234,46 @@ def mla_backward(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset=0, causal=True, sca
             dW_UK[:, h * d_nope:(h + 1) * d_nope] += g["dW_UK_h"]
             dW_UV[:, h * d_v:(h + 1) * d_v] += g["dW_UV_h"]
     return {"dq": dq, "dc_kv": dc_kv, "dk_rope": dk_rope, "dW_UK": dW_UK, "dW_UV": dW_UV}
+
+
+def absorbed_forward(q, c_kv, k_rope, W_UK, W_UV, q_offset=0, causal=True, scale=None, keep=None):
+    """The absorbed MLA form (the variant the LAGA Abstract contrasts with: W_UK is
+    folded into the query and attention runs over the compressed latent):
+
+      q_lat_h = q_nope_h W_UK_h^T,  s = scale ([q_lat_h | q_rope_h] [c_kv | k_rope]^T),
+      ctx_h = softmax(s) c_kv,      out_h = ctx_h W_UV_h.
+
+    Returns out [B,Sq,n_h,d_v] and lse [B,n_h,Sq] (fp64). If `keep` is a dict, the
+    intermediates q_lat and ctx ([B,Sq,n_h,d_c]) are stored in it."""
+    B, Sq, n_h, d_qk = q.shape
+    S, d_c = c_kv.shape[1], c_kv.shape[2]
+    d_nope = W_UK.shape[1] // n_h
+    d_v = W_UV.shape[1] // n_h
+    if scale is None:
+        scale = default_scale(d_nope, d_qk - d_nope)
+    out = np.zeros((B, Sq, n_h, d_v))
+    lse = np.zeros((B, n_h, Sq))
+    q_lat_all = np.zeros((B, Sq, n_h, d_c))
+    ctx_all = np.zeros((B, Sq, n_h, d_c))
+    for b in range(B):
+        key = np.concatenate([_f64(c_kv[b]), _f64(k_rope[b])], axis=1)  # one key for every head
+        for h in range(n_h):
+            q_lat = _f64(q[b, :, h, :d_nope]) @ _f64(W_UK[:, h * d_nope:(h + 1) * d_nope]).T
+            q_abs = np.concatenate([q_lat, _f64(q[b, :, h, d_nope:])], axis=1)
+            s = scale * (q_abs @ key.T)
+            s = np.where(visible_mask(np.arange(Sq), S, q_offset, causal), s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            l = e.sum(axis=1, keepdims=True)
+            ctx = (e / l) @ _f64(c_kv[b])  # attention in the latent space
+            out[b, :, h, :] = ctx @ _f64(W_UV[:, h * d_v:(h + 1) * d_v])
+            lse[b, h, :] = m[:, 0] + np.log(l[:, 0])
+            q_lat_all[b, :, h] = q_lat
+            ctx_all[b, :, h] = ctx
+    if keep is not None:
+        keep["q_lat"] = q_lat_all
+        keep["ctx"] = ctx_all
+    return out, lse
 
 
 def reconstruct(c_kv, W_UK, W_UV, n_h):

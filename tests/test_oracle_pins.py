@@ -111,6 +111,42 @@ def absorbed_forward(p, x, scale):
     return out, lse
 
 
+def test_oracle_absorbed_form_equals_explicit_and_the_test_restatement():
+    """The oracle's absorbed form (used by the GPU absorbed path's parity tests)
+    equals the explicit form and this file's own restatement of the absorbed form,
+    on a causal shard and a non-causal problem; its intermediates have the widths
+    the Abstract describes (n_h x d_c per query row)."""
+    for causal, q_offset in [(True, 5), (False, 0)]:
+        p = small(n_h=3, S=11, Sq=6, q_offset=q_offset, causal=causal)
+        x = inputs64(p, seed=4)
+        keep = {}
+        out, lse = oracle.absorbed_forward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], p.q_offset,
+                                           p.causal, keep=keep)
+        ref_out, ref_lse = run_fwd(p, x)
+        np.testing.assert_allclose(out, ref_out, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-11, atol=1e-12)
+        if causal:
+            o2, l2 = absorbed_forward(p, x, O.default_scale(p.d_nope, p.d_rope))
+            np.testing.assert_allclose(out, o2, rtol=1e-11, atol=1e-12)
+        assert keep["q_lat"].shape == (p.B, p.Sq, p.n_h, p.d_c) and keep["ctx"].shape == (p.B, p.Sq, p.n_h, p.d_c)
+
+
+def test_oracle_absorbed_form_hand_worked():
+    """The hand-worked two-token example of the default-scale test, through the
+    absorbed form: q_lat_1 = q_nope_1 W_UK^T = (0, 2 ln 3) against c_kv = I gives the
+    same scores (0, ln 3) at scale 1/2, so out = (2, 5) and lse = (1, ln 4)."""
+    ln3 = math.log(3.0)
+    x = {"q": np.array([[[[0.0, 0.0, 0.0, 2.0]], [[1.0, 0.0, 0.0, 0.0]]]]),
+         "c_kv": np.array([[[1.0, 0.0], [0.0, 1.0]]]), "k_rope": np.array([[[0.0, 1.0], [0.0, 0.0]]]),
+         "W_UK": np.array([[0.0, 0.0], [2.0 * ln3, 0.0]]), "W_UV": np.array([[2.0], [6.0]])}
+    keep = {}
+    out, lse = oracle.absorbed_forward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], 0, True, keep=keep)
+    np.testing.assert_allclose(out[0, :, 0, 0], [2.0, 5.0], rtol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], [1.0, math.log(4.0)], rtol=1e-14)
+    np.testing.assert_allclose(keep["q_lat"][0, 1, 0], [0.0, 2.0 * ln3], rtol=1e-14)
+    np.testing.assert_allclose(keep["ctx"][0, 1, 0], [0.25, 0.75], rtol=1e-14)
+
+
 @pytest.mark.parametrize("seed", [0, 7])
 def test_absorbed_form_equals_explicit(seed):
     p = small(n_h=3, S=11, Sq=6, q_offset=5)

@@ -440,3 +440,54 @@ def test_determinism():
     # no atomics anywhere: every output is produced in a fixed order
     for k in ("out", "lse", "dq", "dc_kv", "dk_rope", "dW_UK", "dW_UV"):
         assert torch.equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------------ the absorbed form (comparison path)
+ABSORBED_CASES = {
+    "aligned": small(n_h=2, Sq=256, S=256),
+    "ragged_offset": small(B=2, n_h=3, Sq=200, S=520, q_offset=300),
+    "noncausal_ragged": small(n_h=2, Sq=77, S=333, causal=False),
+    "single_query_last": small(Sq=1, S=701, q_offset=700),
+    "multi_tile": small(B=1, n_h=2, Sq=384, S=1000, q_offset=600),
+}
+
+
+@pytest.mark.parametrize("name", list(ABSORBED_CASES))
+def test_absorbed_forward(name):
+    """laga_mla_absorbed_fwd (q_lat GEMM, latent-space attention, output GEMM) against
+    the oracle's absorbed form, and its out / lse against the explicit form's."""
+    p = ABSORBED_CASES[name]
+    x = make_inputs(p, seed=20)
+    t = to_dev(x, p)
+    out, lse = laga.absorbed_fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, p.causal)
+    laga.check(dev())
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    ref_out, ref_lse = oracle.absorbed_forward(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"],
+                                               p.q_offset, p.causal)
+    assert_close({"out": out, "lse": lse}, {"out": ref_out, "lse": ref_lse}, TOL["bf16"], tag=f"absorbed {name}")
+
+
+def test_absorbed_forward_dsv3_sampled_heads():
+    """The absorbed form on the DeepSeek-V3 SP=8 last-rank shard: sampled heads against
+    the per-head oracle (out and lse are the explicit form's)."""
+    p = DSV3_LAST_RANK
+    x = make_inputs(p, seed=2009, with_dout=False)
+    t = to_dev(x, p)
+    out, lse = laga.absorbed_fwd(t["q"], t["c_kv"], t["k_rope"], t["W_UK"], t["W_UV"], p.q_offset, True)
+    laga.check(dev())
+    x64 = {k: v.astype(np.float64) for k, v in x.items()}
+    for h in (0, 127):
+        ro, rl = oracle.mla_forward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], 0, h,
+                                         p.q_offset, True)
+        assert_close({"out": out[0, :, h], "lse": lse[0, h]}, {"out": ro, "lse": rl}, TOL["bf16"],
+                     tag=f"absorbed dsv3 head {h}")
+
+
+def test_absorbed_forward_rejects_two_segments():
+    p = TC_CASES["two_segments"]
+    assert laga.absorbed_workspace_bytes(p) == 0
+    d = laga.make_desc(p)
+    L = laga.lib()
+    import ctypes
+    fake = ctypes.c_void_p(4096)
+    assert L.laga_mla_absorbed_fwd(ctypes.byref(d), *([fake] * 8), 1 << 30, None) == 2
