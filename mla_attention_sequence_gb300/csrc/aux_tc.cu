@@ -47,41 +47,47 @@ namespace {
 
 constexpr float LOG2E = 1.4426950408889634f;
 
-// One warp per (b, h, i) row of the padded [B][n_h][sq_pad] arrays.
+__device__ __forceinline__ uint32_t pack_bf16x2_dev(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Half a warp per (b, h, i) row of the padded [B][n_h][sq_pad] arrays: 16 lanes
+// x 8 values of out and dout each, as 16-byte loads.
 __global__ void bwd_pre_kernel(Dims d, const bf16* __restrict__ out, const bf16* __restrict__ dout,
                                const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta) {
-  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
   const long long rows = static_cast<long long>(d.B) * d.n_h * d.sq_pad;
-  if (row >= rows) return;
-  const int lane = threadIdx.x & 31;
-  const int i = static_cast<int>(row % d.sq_pad);
-  const long long bh = row / d.sq_pad;
+  const int l16 = threadIdx.x & 15;
+  const bool in = row < rows;  // every lane stays for the shuffles below
+  const int i = in ? static_cast<int>(row % d.sq_pad) : 0;
+  const long long bh = in ? row / d.sq_pad : 0;
   const int h = static_cast<int>(bh % d.n_h);
   const int b = static_cast<int>(bh / d.n_h);
-  if (i >= d.Sq) {
-    if (lane == 0) {
+  float acc = 0.f;
+  if (in && i < d.Sq) {
+    const long long off = ((static_cast<long long>(b) * d.Sq + i) * d.n_h + h) * 128 + l16 * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(out + off);
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 af = __bfloat1622float2(a2[k]);
+      const float2 gf = __bfloat1622float2(g2[k]);
+      acc = fmaf(af.x, gf.x, acc);
+      acc = fmaf(af.y, gf.y, acc);
+    }
+  }
+  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (in && l16 == 0) {
+    if (i >= d.Sq) {
       lse2[row] = INFINITY;
       delta[row] = 0.f;
+    } else {
+      delta[row] = acc;
+      lse2[row] = lse[(static_cast<long long>(b) * d.n_h + h) * d.Sq + i] * LOG2E;
     }
-    return;
-  }
-  const long long off = ((static_cast<long long>(b) * d.Sq + i) * d.n_h + h) * 128 + lane * 4;
-  const uint2 a = *reinterpret_cast<const uint2*>(out + off);
-  const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
-  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
-  float acc = 0.f;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float2 af = __bfloat1622float2(a2[k]);
-    const float2 gf = __bfloat1622float2(g2[k]);
-    acc = fmaf(af.x, gf.x, acc);
-    acc = fmaf(af.y, gf.y, acc);
-  }
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    delta[row] = acc;
-    lse2[row] = lse[(static_cast<long long>(b) * d.n_h + h) * d.Sq + i] * LOG2E;
   }
 }
 
@@ -106,11 +112,9 @@ __global__ void rope_sum_kernel(Dims d, const float* __restrict__ dkr, bf16* __r
       acc.w += v.w;
     }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 o;
-  o.x = *reinterpret_cast<uint32_t*>(&lo);
-  o.y = *reinterpret_cast<uint32_t*>(&hi);
+  o.x = pack_bf16x2_dev(acc.x, acc.y);
+  o.y = pack_bf16x2_dev(acc.z, acc.w);
   reinterpret_cast<uint2*>(dk_rope + (static_cast<long long>(b) * d.S + j) * 64)[c4] = o;
 }
 
@@ -120,7 +124,7 @@ LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const 
                         cudaStream_t st) {
   LaunchResult r;
   const long long rows = static_cast<long long>(d.B) * d.n_h * d.sq_pad;
-  bwd_pre_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(d, out, dout, lse, w.lse2, w.delta);
+  bwd_pre_kernel<<<static_cast<unsigned>((rows + 15) / 16), 256, 0, st>>>(d, out, dout, lse, w.lse2, w.delta);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "bwd_pre_kernel";
   return r;
