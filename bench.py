@@ -408,6 +408,10 @@ def run_ours(args, name: str):
     out_done = [torch.cuda.Event() for _ in range(2)]
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
+    # the compute of each step inside the end-to-end loop, to tell copy/compute
+    # interference (compute slower) from dependency stalls (gaps between steps)
+    c_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    c_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     e_start.record(stream)
@@ -425,8 +429,10 @@ def run_ours(args, name: str):
         stream.wait_event(in_ready[b])
         if i >= 2:
             stream.wait_event(out_done[b])  # step i-2's results have left this set
+        c_start[i].record(stream)
         for buf in sbufs:
             laga.step(buf, args.variant)
+        c_end[i].record(stream)
         done[b].record(stream)
         copy_out.wait_event(done[b])
         with torch.cuda.stream(copy_out):
@@ -442,6 +448,7 @@ def run_ours(args, name: str):
     barrier(world)
     laga.check(dev)
     e2e_ms = reduce_max(e_start.elapsed_time(e_end), world, dev)
+    e2e_compute_ms = float(np.mean([a.elapsed_time(z) for a, z in zip(c_start, c_end)]))
 
     flops = sum(p.flops_step() for p in problems)
     tokens = sum(p.B * p.Sq for p in problems)
@@ -504,6 +511,7 @@ def run_ours(args, name: str):
             "roofline": roof,
             "kernels_ms_per_launch": kernel_ms,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "compute_ms_per_step": e2e_compute_ms,
                     "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": gpu_launches,
             "clocks": clk,
