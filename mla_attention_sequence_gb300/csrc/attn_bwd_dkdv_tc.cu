@@ -113,9 +113,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto ds_full = [bars](int i) { return (i & 1) ? bars + 17 : bars + 12; };
   uint64_t* acc_done = bars + 13;
   uint64_t* drain = bars + 14;
-  uint64_t* epi_full = bars + 15;  // epilogue tiles staged in shared memory
   uint64_t* dp_free = bars + 16;   // dP^T(i) read into registers: dP(i+1) may overwrite it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  // epilogue box k (16 KB) staged in shared memory; the waiter stores each as soon
+  // as it is complete, so the boxes' read-out overlaps the staging of the next
+  auto box_full = [bars](int k) { return bars + 19 + k; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(dp_free, SOFTMAX_WARPS);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    mbar_init(epi_full, SOFTMAX_WARPS);
+    for (int k = 0; k < 6; ++k) mbar_init(box_full(k), k == 2 ? SOFTMAX_WARPS : SOFTMAX_WARPS / 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -238,16 +240,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool w = warp_wait_or_abort(bar, parity, abort_flag, where);
       return bar_and(HANDOFF_BAR, 64, w);
     };
-    if (handoff(kv_full, 0, 52)) {
+    bool all_ok = handoff(kv_full, 0, 52);
+    if (all_ok) {
       for (int i = -2; i < n_qt; ++i) {
         if (i >= 0) {
-          if (!handoff(&p_full[i & 1], (i >> 1) & 1, 54)) break;
-          if (i + 1 < n_qt && !handoff(dp_free, i & 1, 56)) break;
-          if (!handoff(ds_full(i), (i >> 1) & 1, 55)) break;
+          if (!handoff(&p_full[i & 1], (i >> 1) & 1, 54)) { all_ok = false; break; }
+          if (i + 1 < n_qt && !handoff(dp_free, i & 1, 56)) { all_ok = false; break; }
+          if (!handoff(ds_full(i), (i >> 1) & 1, 55)) { all_ok = false; break; }
         }
-        if (i + 2 < n_qt && !handoff(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, 53)) break;
+        if (i + 2 < n_qt && !handoff(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, 53)) {
+          all_ok = false;
+          break;
+        }
       }
     }
+    // Epilogue stores, one 16 KB box at a time in the order the boxes complete
+    // (warpgroup 0 stages boxes 0, 1 and half of 2; warpgroup 1 boxes 3, 4, 5 and
+    // the other half of 2). The tensor-map store reads a box out of shared memory
+    // at ~28 B/clk; issued box by box, that overlaps the staging of the others.
+    if (all_ok && lane == 0) {
+      const int row = b * p.skv_pad + kv0;
+      for (int j = 0; j < 6; ++j) {
+        const int k = j == 0 ? 0 : j == 1 ? 3 : j == 2 ? 1 : j == 3 ? 4 : j == 4 ? 5 : 2;
+        if (!mbar_wait_or_abort(box_full(k), 0, abort_flag, 65)) break;
+        uint8_t* box = smem + OFF_STAGE + k * 16384;
+        if (k < 2) tma_store_2d(&mdV, box, h * 128 + 64 * k, row);
+        else if (k < 4) tma_store_2d(&mdK, box, h * 128 + 64 * (k - 2), row);
+        else tma_store_2d(&mdKR, box, h * 64 + 32 * (k - 4), row);
+        bulk_commit_group();
+      }
+      bulk_wait_read_all();  // the staging memory is read out; the writes finish on their own
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // The whole warp runs the issue loop (an elected lane issues each block of MMAs).
     // Readiness comes from the waiter through the named barrier, never from a
@@ -461,8 +485,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // TMEM columns: dV 0..127, dK 128..319 (no-RoPE 128..255, RoPE 256..319);
       // warpgroup 0 reads chunks 0..4, warpgroup 1 chunks 5..9 (32 columns each)
       uint8_t* stg = smem + OFF_STAGE;
+      // warpgroup 0: chunks 0, 1 (box 0), 2, 3 (box 1), 4 (box 2);
+      // warpgroup 1: chunks 6, 7 (box 3), 8 (box 4), 9 (box 5), 5 (box 2)
 #pragma unroll 1
-      for (int c = 5 * half; c < 5 * half + 5; ++c) {
+      for (int j = 0; j < 5; ++j) {
+        const int c = half == 0 ? j : (j < 4 ? 6 + j : 5);
         uint32_t u[32];
         tmem_ld32(tmem + lane_off + c * 32, u);
         tmem_wait_ld();
@@ -470,6 +497,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) u[k] = 0u;
         }
+        int done_box = -1;  // the box this chunk completes (for this warpgroup)
         if (c < 8) {
           const float sc = c < 4 ? 1.f : p.scale;
           uint8_t* box = stg + (c >> 1) * 16384;
@@ -482,6 +510,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * sc, __uint_as_float(u[8 * v + 7]) * sc);
             *reinterpret_cast<uint4*>(box + sw128_offset(r, (c & 1) * 4 + v)) = w;
           }
+          if ((c & 1) == 1 || c == 4) done_box = c >> 1;  // chunk 5 completes box 2 for warpgroup 1
         } else {
           uint8_t* box = stg + (4 + c - 8) * 16384;
 #pragma unroll
@@ -493,21 +522,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             w.w = __float_as_uint(__uint_as_float(u[4 * v + 3]) * p.scale);
             *reinterpret_cast<uint4*>(box + sw128_offset(r, v)) = w;
           }
+          done_box = 4 + c - 8;
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(epi_full);
-      if (warp == 2 && lane == 0 && mbar_wait_or_abort(epi_full, 0, abort_flag, 65)) {
-        const int row = b * p.skv_pad + kv0;
-        tma_store_2d(&mdV, stg, h * 128, row);
-        tma_store_2d(&mdV, stg + 16384, h * 128 + 64, row);
-        tma_store_2d(&mdK, stg + 2 * 16384, h * 128, row);
-        tma_store_2d(&mdK, stg + 3 * 16384, h * 128 + 64, row);
-        tma_store_2d(&mdKR, stg + 4 * 16384, h * 64, row);
-        tma_store_2d(&mdKR, stg + 5 * 16384, h * 64 + 32, row);
-        bulk_commit_group();
-        bulk_wait_read_all();  // the staging memory is read out; the writes finish on their own
+        if (done_box >= 0) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(box_full(done_box));
+        }
       }
     }
   }
