@@ -68,9 +68,15 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
   n = r / gm;
 }
 
-template <int MODE, int BN, int STAGES>
+// MH = 2 makes a tile 256 rows tall: two M = 128 products per K16 step share
+// each B k-block, so a stage streams 64 KB per 1024 tensor cycles (64 B/clk)
+// instead of 48 KB per 512 (94 B/clk). Its two accumulators fill TMEM, so the
+// epilogue of a tile does not overlap the next one's main loop; that costs
+// little where the k loop is long (DCKV, DW).
+template <int MODE, int BN, int STAGES, int MH = 1>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_HALF = BM * BK * 2;
+  static constexpr int A_BYTES = MH * A_HALF;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_BYTES = 256;
@@ -78,21 +84,24 @@ struct Cfg {
   static constexpr int EPI_BOX = 32 * 64;
   static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int NACC = (2 * MH * BN <= 512) ? 2 : 1;  // accumulator sets in TMEM
+  static constexpr uint32_t TMEM_COLS = NACC * MH * BN;
   static constexpr bool A_MN = (MODE == DW);
   static constexpr bool B_MN = (MODE != DCKV && MODE != QLAT);
   static constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
-  static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
+  static_assert(TMEM_COLS <= 512, "the accumulators must fit in TMEM");
   static_assert(BN % 64 == 0 && BN <= 256, "BN");
+  static_assert(MH == 1 || MODE == DCKV || MODE == DW, "256-row tiles serve the long-k GEMMs");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MH>
 __global__ void __launch_bounds__(224, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
                    const __grid_constant__ CUtensorMap mapO0, const __grid_constant__ CUtensorMap mapO1,
                    const GemmParams p) {
-  using C = Cfg<MODE, BN, STAGES>;
+  using C = Cfg<MODE, BN, STAGES, MH>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -179,8 +188,8 @@ __global__ void __launch_bounds__(224, 1)
           } else if constexpr (MODE == DCKV) {
             const bool second = kb >= p.kb_first;
             const int kk = second ? kb - p.kb_first : kb;
-            if (load_a)
-              tma_load_2d(a, second ? &mapA1 : &mapA0, &full[s], kk * BK, b * p.skv_pad + m * BM);
+            if (load_a)  // one [BM*MH rows][64] box
+              tma_load_2d(a, second ? &mapA1 : &mapA0, &full[s], kk * BK, b * p.skv_pad + m * BM * MH);
             else
               tma_load_2d(bsm, second ? &mapB1 : &mapB0, &full[s], kk * BK, n * BN);
           } else if constexpr (MODE == QLAT) {
@@ -206,8 +215,9 @@ __global__ void __launch_bounds__(224, 1)
             const int bb = kb / p.kb_per_batch;
             const int kk = kb - bb * p.kb_per_batch;
             if (load_a) {
-              tma_load_2d(a, &mapA0, &full[s], m * BM, bb * p.S + kk * BK);
-              tma_load_2d(a + 8192, &mapA0, &full[s], m * BM + 64, bb * p.S + kk * BK);
+#pragma unroll
+              for (int i = 0; i < 2 * MH; ++i)
+                tma_load_2d(a + i * 8192, &mapA0, &full[s], m * BM * MH + 64 * i, bb * p.S + kk * BK);
             } else {
               const CUtensorMap* mb = second ? &mapB1 : &mapB0;
 #pragma unroll
@@ -237,14 +247,14 @@ __global__ void __launch_bounds__(224, 1)
     const uint64_t a_desc0 = sdesc_sw128(smem_u32(sA), C::A_MN ? 8192 : 16, 1024);
     const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), C::B_MN ? 8192 : 16, 1024);
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
-      const int buf = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int buf = local % C::NACC;
+      const uint32_t use = static_cast<uint32_t>(local / C::NACC);
       if (!warp_wait_token(&acc_empty[buf], (use & 1) ^ 1, ta, abort_flag, 2)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + buf * BN;
+      const uint32_t d_tmem = tmem_base + buf * MH * BN;
       for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
         const int s = it % STAGES;
         if (!warp_wait_token(&full[s], (it / STAGES) & 1, tf, abort_flag, 3)) {
@@ -258,13 +268,21 @@ __global__ void __launch_bounds__(224, 1)
         // the k-block's four K16 steps as two pairs, the next barriers tested between them
         constexpr uint32_t DA = (C::A_MN ? 2048 : 32) >> 4, DB = (C::B_MN ? 2048 : 32) >> 4;
         static_assert(BK == 64, "four K16 steps per k-block");
-        mma2_ss_warp(d_tmem, a_stage, a_stage + DA, b_stage, b_stage + DB, C::IDESC, kb != 0 ? 1u : 0u);
+        // with MH = 2 each pair runs on both 128-row halves (A and D offset, B shared)
+        constexpr uint32_t DH = C::A_HALF >> 4;
+#pragma unroll
+        for (int h = 0; h < MH; ++h)
+          mma2_ss_warp(d_tmem + h * BN, a_stage + h * DH, a_stage + h * DH + DA, b_stage, b_stage + DB, C::IDESC,
+                       kb != 0 ? 1u : 0u);
         tf = mbar_test(&full[(it + 1) % STAGES], ((it + 1) / STAGES) & 1);
         if (kb == p.k_blocks - 1) {
           const int nl = local + 1;
-          ta = mbar_test(&acc_empty[nl & 1], ((static_cast<uint32_t>(nl >> 1)) & 1) ^ 1);
+          ta = mbar_test(&acc_empty[nl % C::NACC], ((static_cast<uint32_t>(nl / C::NACC)) & 1) ^ 1);
         }
-        mma2_ss_warp(d_tmem, a_stage + 2 * DA, a_stage + 3 * DA, b_stage + 2 * DB, b_stage + 3 * DB, C::IDESC, 1u);
+#pragma unroll
+        for (int h = 0; h < MH; ++h)
+          mma2_ss_warp(d_tmem + h * BN, a_stage + h * DH + 2 * DA, a_stage + h * DH + 3 * DA, b_stage + 2 * DB,
+                       b_stage + 3 * DB, C::IDESC, 1u);
         issued = true;
         mma_commit_warp(&empty[s]);
       }
@@ -295,8 +313,8 @@ __global__ void __launch_bounds__(224, 1)
     int local = 0;
     int chunk = 0;  // chunks stored by this warp so far (buffer = chunk & 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-      const int buf = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int buf = local % C::NACC;
+      const uint32_t use = static_cast<uint32_t>(local / C::NACC);
       bool ok = true;
       if (lane == 0) ok = mbar_wait_or_abort(&acc_full[buf], use & 1, abort_flag, 4);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -314,35 +332,38 @@ __global__ void __launch_bounds__(224, 1)
         omap = second ? map1 : map0;
         n0 = (second ? n - p.n_tiles_first : n) * BN;
       }
-      const int y0 = m * BM + quarter * 32;  // first row of this warp's boxes
-      const uint32_t t_row = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
-        uint32_t r[32];
-        tmem_ld32(t_row + c0, r);
-        tmem_wait_ld();
-        if (c0 + 32 == BN) {  // the accumulator has been read out: the MMA may reuse it
-          tc_fence_before();
+      for (int h = 0; h < MH; ++h) {
+        const int y0 = (m * MH + h) * BM + quarter * 32;  // first row of this warp's boxes
+        const uint32_t t_row = tmem_base + (buf * MH + h) * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
+          uint32_t r[32];
+          tmem_ld32(t_row + c0, r);
+          tmem_wait_ld();
+          if (h == MH - 1 && c0 + 32 == BN) {  // the accumulator has been read out: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          }
+          uint8_t* box = ebuf + (chunk & 1) * C::EPI_BOX;
+          if (lane == 0) bulk_wait_read_1();  // the store that last read this buffer is done reading
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        }
-        uint8_t* box = ebuf + (chunk & 1) * C::EPI_BOX;
-        if (lane == 0) bulk_wait_read_1();  // the store that last read this buffer is done reading
-        __syncwarp();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-          w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-          w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-          w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-          *reinterpret_cast<uint4*>(box + sw64_offset(lane, v)) = w;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(omap, box, n0 + c0, y0, b);
-          bulk_commit_group();
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+            *reinterpret_cast<uint4*>(box + sw64_offset(lane, v)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(omap, box, n0 + c0, y0, b);
+            bulk_commit_group();
+          }
         }
       }
       if (MODE == RECON_FWD && lane == 0 && local < 512) LAGA_TRACE_POINT(gemm, 10, local);
@@ -359,13 +380,13 @@ __global__ void __launch_bounds__(224, 1)
   }
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MH = 1>
 LaunchResult launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                          const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1, const GemmParams& p,
                          cudaStream_t st) {
-  using C = Cfg<MODE, BN, STAGES>;
+  using C = Cfg<MODE, BN, STAGES, MH>;
   LaunchResult r;
-  auto kern = gemm_tc_kernel<MODE, BN, STAGES>;
+  auto kern = gemm_tc_kernel<MODE, BN, STAGES, MH>;
   r.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (r.err != cudaSuccess) {
     r.what = "cudaFuncSetAttribute(gemm)";
@@ -457,15 +478,19 @@ LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, con
 
 LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws, const bf16* W_UK,
                              const bf16* W_UV, bf16* dc_kv, cudaStream_t st) {
-  // N = 256 halves the operand bytes per MMA cycle against N = 128 (the k-blocks
-  // stream 48 KB per 512 tensor cycles instead of 32 KB per 256).
+  // 256 x 256 tiles (two 128-row halves) stream 64 KB per 1024 tensor cycles;
+  // 128 x 256 ones 48 KB per 512 and 128 x 128 ones 32 KB per 256. The k loop is
+  // n_h * 256 long, so the unoverlapped epilogue of a 256-row tile is cheap.
+  // A last 256-row tile that runs past a batch element's padded rows reads the
+  // next element's (or zero-filled) rows; the output map clips those rows.
   const int BN = d.d_c % 256 == 0 ? 256 : 128;
+  const int MH = BN == 256 ? 2 : 1;
   LaunchResult r;
   CUtensorMap a0, a1, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;  // reduction length of each pair
   const uint64_t rows = static_cast<uint64_t>(d.B) * d.skv_pad;
-  r.cu = tmap_bf16_2d(&a0, dk_ws, N, rows, N * 2, 64, 128);
-  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&a1, dv_ws, N, rows, N * 2, 64, 128);
+  r.cu = tmap_bf16_2d(&a0, dk_ws, N, rows, N * 2, 64, 128 * MH);
+  if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&a1, dv_ws, N, rows, N * 2, 64, 128 * MH);
   if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b0, W_UK, N, d.d_c, N * 2, 64, BN);
   if (r.cu == CUDA_SUCCESS) r.cu = tmap_bf16_2d(&b1, W_UV, N, d.d_c, N * 2, 64, BN);
   if (r.cu != CUDA_SUCCESS) {
@@ -473,7 +498,7 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
     return r;
   }
   GemmParams p{};
-  p.m_tiles = d.skv_pad / BM;
+  p.m_tiles = (d.skv_pad + BM * MH - 1) / (BM * MH);
   p.n_tiles = d.d_c / BN;
   p.n_tiles_first = p.n_tiles;
   p.batches = d.B;
@@ -487,19 +512,24 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
   p.out_batch_stride = static_cast<long long>(d.S) * d.d_c;
   p.rows_valid = d.S;
   CUtensorMap o0;
-  r.cu = tmap_out(&o0, dc_kv, static_cast<uint64_t>(d.d_c), static_cast<uint64_t>(d.S), static_cast<uint64_t>(d.B),
-                  static_cast<uint64_t>(d.S) * d.d_c);
+  // Rows at or past the padded visible prefix are clipped: a 256-row tile may
+  // overhang it, and the caller zero-fills those rows of dc_kv.
+  r.cu = tmap_out(&o0, dc_kv, static_cast<uint64_t>(d.d_c), static_cast<uint64_t>(std::min(d.S, d.skv_pad)),
+                  static_cast<uint64_t>(d.B), static_cast<uint64_t>(d.S) * d.d_c);
   if (r.cu != CUDA_SUCCESS) {
     r.what = "tensor map dc_kv out";
     return r;
   }
-  if (BN == 256) return launch_gemm<DCKV, 256, 4>(a0, a1, b0, b1, o0, o0, p, st);
+  if (BN == 256) return launch_gemm<DCKV, 256, 3, 2>(a0, a1, b0, b1, o0, o0, p, st);
   return launch_gemm<DCKV, 128, 6>(a0, a1, b0, b1, o0, o0, p, st);
 }
 
 LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws, const bf16* dv_ws, bf16* dW_UK,
                              bf16* dW_UV, cudaStream_t st) {
+  // 256-row tiles (two halves sharing each B k-block) when d_c allows them: the
+  // k loop is B * S long, so the unoverlapped epilogue of such a tile is cheap.
   const int BN = (d.n_h % 2 == 0) ? 256 : 128;
+  const int MH = (BN == 256 && d.d_c % 256 == 0) ? 2 : 1;
   LaunchResult r;
   CUtensorMap a0, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;
@@ -513,7 +543,7 @@ LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws,
     return r;
   }
   GemmParams p{};
-  p.m_tiles = d.d_c / BM;
+  p.m_tiles = d.d_c / (BM * MH);
   p.n_tiles_first = static_cast<int>(N / BN);
   p.n_tiles = 2 * p.n_tiles_first;
   p.batches = 1;
@@ -533,6 +563,7 @@ LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws,
     r.what = "tensor map dW out";
     return r;
   }
+  if (MH == 2) return launch_gemm<DW, 256, 3, 2>(a0, a0, b0, b1, o0, o1, p, st);
   if (BN == 256) return launch_gemm<DW, 256, 4>(a0, a0, b0, b1, o0, o1, p, st);
   return launch_gemm<DW, 128, 6>(a0, a0, b0, b1, o0, o1, p, st);
 }
