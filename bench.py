@@ -180,18 +180,27 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 def oracle_sample(p: Problem, x: dict, heads: list[int], keep: dict | None = None):
-    """Run the fp64 oracle's forward+backward for the given heads of batch 0.
-    Returns the algorithmic flops of that sample; `keep` (if given) collects each
-    head's results by head index."""
+    """Run the fp64 oracle's forward+backward for the given heads, over every
+    batch element. Returns the algorithmic flops of that sample; `keep` (if
+    given) collects each head's results by head index: batch 0's per-row outputs
+    (out, lse, dq) and the head's weight gradients summed over the batch, as the
+    library's dW_UK / dW_UV are."""
     import oracle
     x64 = x if all(v.dtype == np.float64 for v in x.values()) else {k: v.astype(np.float64) for k, v in x.items()}
     pos = oracle.query_positions(p.Sq, p.q_offset, p.q_split, p.q_offset2) if p.q_split > 0 else p.q_offset
     for h in heads:
-        g = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"], x64["dout"], 0,
-                                     h, pos, p.causal)
+        g = None
+        for bi in range(p.B):
+            gb = oracle.mla_backward_head(x64["q"], x64["c_kv"], x64["k_rope"], x64["W_UK"], x64["W_UV"],
+                                          x64["dout"], bi, h, pos, p.causal)
+            if g is None:
+                g = gb
+            else:
+                g["dW_UK_h"] = g["dW_UK_h"] + gb["dW_UK_h"]
+                g["dW_UV_h"] = g["dW_UV_h"] + gb["dW_UV_h"]
         if keep is not None:
             keep[h] = g
-    return p.with_(n_h=len(heads), B=1).flops_step()
+    return p.with_(n_h=len(heads)).flops_step()
 
 
 def time_oracle(p: Problem, x: dict, budget_s: float = 15.0, max_heads: int = 64, keep: dict | None = None):
@@ -209,7 +218,7 @@ def time_oracle(p: Problem, x: dict, budget_s: float = 15.0, max_heads: int = 64
 
 def sampled_errors(p: Problem, buf, ref_heads: dict) -> dict:
     """max|gpu - oracle| / max|oracle| per output tensor over the oracle's sampled
-    heads of batch 0 (the per-head outputs: out, lse, dq, dW_UK, dW_UV)."""
+    heads (out, lse, dq of batch 0; dW_UK, dW_UV summed over the batch)."""
     acc = {}
     for h, g in ref_heads.items():
         pairs = {"out": (buf.out[0, :, h], g["out_h"]), "lse": (buf.lse[0, h], g["lse_h"]),
@@ -257,7 +266,7 @@ def run_reference(args, p: Problem):
         "config": workload_config(p, {"sample": f"{heads_per_step} head(s) of {p.n_h} per step"}),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"fp64 oracle fwd+bwd of {heads_per_step} head per step (of {p.n_h}), "
-                                   f"batch 0 of the shard; TFLOP/s of that sample's algorithmic flops"},
+                                   f"every batch element of the shard; TFLOP/s of that sample's algorithmic flops"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -91,3 +91,28 @@ def test_reference_arm_only_rank0_prints():
     assert out[0][0] == 0 and out[1][0] == 0
     assert json.loads(out[0][1].strip())["impl"] == "reference"
     assert out[1][1].strip() == ""
+
+
+def test_oracle_sample_weight_gradients_sum_over_the_batch():
+    """The bench's sampled-error reference: per sampled head, batch 0's out / lse
+    / dq rows and the head's dW_UK / dW_UV columns summed over every batch
+    element (the library's weight gradients are batch sums), checked against the
+    oracle's full forward and backward on a B = 2 problem."""
+    import numpy as np
+    import oracle
+    from mla_attention_sequence_gb300.configs import Problem
+    from mla_attention_sequence_gb300.synth import make_inputs
+    p = Problem(B=2, Sq=6, S=11, n_h=3, d_c=8, d_nope=4, d_rope=2, d_v=5, q_offset=5, dtype="f32")
+    x = {k: v.astype(np.float64) for k, v in make_inputs(p, seed=3).items()}
+    keep = {}
+    flops = bench.oracle_sample(p, x, [0, 2], keep)
+    assert flops == p.with_(n_h=2).flops_step()
+    g = oracle.mla_backward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], x["dout"], p.q_offset, True)
+    out, lse = oracle.mla_forward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], p.q_offset, True)
+    for h in (0, 2):
+        k = keep[h]
+        np.testing.assert_allclose(k["dW_UK_h"], g["dW_UK"][:, h * 4:(h + 1) * 4], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(k["dW_UV_h"], g["dW_UV"][:, h * 5:(h + 1) * 5], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(k["dq_h"], g["dq"][0, :, h], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(k["out_h"], out[0, :, h], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(k["lse_h"], lse[0, h], rtol=1e-12, atol=1e-14)
