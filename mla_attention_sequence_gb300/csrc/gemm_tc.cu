@@ -695,6 +695,20 @@ CUresult tmap_out(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
 
 }  // namespace
 
+// Tile shape of the long-k GEMMs (dc_kv, dW): 256 x 256 tiles (MH = 2) move the
+// fewest operand bytes per MMA but give few tiles; on small problems they leave
+// most SMs idle. Take the widest shape whose tile count still fills about three
+// quarters of the SMs: 256 x 256, else 128 x 256, else 128 x 128.
+struct LongKShape {
+  int MH, BN;
+};
+LongKShape long_k_shape(long long tiles_256x256, bool mh2_ok) {
+  const long long fill = (3LL * sm_count()) / 4;
+  if (mh2_ok && tiles_256x256 >= fill) return {2, 256};
+  if (2 * tiles_256x256 >= fill) return {1, 256};
+  return {1, 128};
+}
+
 LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, const bf16* W_UV, bf16* k_ws,
                           bf16* v_ws, int rows_pad, cudaStream_t st) {
   LaunchResult r;
@@ -758,8 +772,10 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
   // n_h * 256 long, so the unoverlapped epilogue of a 256-row tile is cheap.
   // A last 256-row tile that runs past a batch element's padded rows reads the
   // next element's (or zero-filled) rows; the output map clips those rows.
-  const int BN = d.d_c % 256 == 0 ? 256 : 128;
-  const int MH = BN == 256 ? 2 : 1;
+  LongKShape shape{1, 128};
+  if (d.d_c % 256 == 0)
+    shape = long_k_shape(static_cast<long long>(d.B) * ((d.skv_pad + 255) / 256) * (d.d_c / 256), true);
+  const int BN = shape.BN, MH = shape.MH;
   LaunchResult r;
   CUtensorMap a0, a1, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;  // reduction length of each pair
@@ -795,7 +811,8 @@ LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws
     r.what = "tensor map dc_kv out";
     return r;
   }
-  if (BN == 256) return launch_gemm<DCKV, 256, 3, 2>(a0, a1, b0, b1, o0, o0, p, st);
+  if (MH == 2) return launch_gemm<DCKV, 256, 3, 2>(a0, a1, b0, b1, o0, o0, p, st);
+  if (BN == 256) return launch_gemm<DCKV, 256, 4>(a0, a1, b0, b1, o0, o0, p, st);
   return launch_gemm<DCKV, 128, 6>(a0, a1, b0, b1, o0, o0, p, st);
 }
 
@@ -803,8 +820,10 @@ LaunchResult tc_recon_bwd_dw(const Dims& d, const bf16* c_kv, const bf16* dk_ws,
                              bf16* dW_UV, cudaStream_t st) {
   // 256-row tiles (two halves sharing each B k-block) when d_c allows them: the
   // k loop is B * S long, so the unoverlapped epilogue of such a tile is cheap.
-  const int BN = (d.n_h % 2 == 0) ? 256 : 128;
-  const int MH = (BN == 256 && d.d_c % 256 == 0) ? 2 : 1;
+  LongKShape shape{1, 128};
+  if (d.n_h % 2 == 0)
+    shape = long_k_shape(static_cast<long long>(d.d_c / 256) * 2 * (d.n_h / 2), d.d_c % 256 == 0);
+  const int BN = shape.BN, MH = shape.MH;
   LaunchResult r;
   CUtensorMap a0, b0, b1;
   const uint64_t N = static_cast<uint64_t>(d.n_h) * 128;
