@@ -2,15 +2,26 @@
 // gradient, on the tensor cores (d_qk = 128 + 64, d_v = 128, bf16 operands,
 // fp32 accumulation).
 //
-// One CTA per (128-row key tile, head, batch element); it walks the 64-row
-// query tiles that can see its keys. Keys sit on the TMEM lanes:
+// One CTA per (128-row key tile, group of G consecutive heads, batch element);
+// for each head of its group in turn it walks the 64-row query tiles that can
+// see its keys. Keys sit on the TMEM lanes:
 //   S^T  = K Q^T          P^T  = exp(S^T * scale - lse)
 //   dP^T = V dO^T         dS^T = P^T o (dP^T - D)
 //   dV  += P^T dO         dK  += dS^T Q        (scale applied once at the end)
 // P^T and dS^T are written back into TMEM as packed bf16 over S^T / dP^T and
 // feed the dV / dK products as the A operand straight from TMEM, so they never
 // touch shared memory. dK covers all 192 head dims in one N = 192 product: the
-// first 128 columns are dK_nope, the last 64 this head's RoPE-key gradient.
+// first 128 columns are dK_nope, the last 64 the RoPE-key gradient, which is one
+// tensor shared by every head: those columns keep accumulating over the group's
+// G heads and are written once per CTA (fp32, one partial per head group).
+//
+// Head boundaries. A CTA pays its start (TMEM, barriers, the first tiles' load
+// latency) once for G heads. When head u's last dP^T has been issued, the MMA
+// warp releases the key/value tile (kv_empty) and the producer loads head u+1's
+// K_nope and V over it (the RoPE key stays); when head u's last dK has finished
+// (acc_done), the key-row warps move dV and dK_nope from TMEM to global memory,
+// zero the dK_nope columns and release the accumulators (acc_free) for head u+1's
+// first dV, while the tensor pipe already runs head u+1's first S^T and dP^T.
 //
 // Warp roles (352 threads):
 //   warp 0      lane 0: TMA for the key/value tile, then Q, dO, lse, D tiles
@@ -23,7 +34,8 @@
 //               compute warps share its SM sub-partition; the named barrier
 //               costs it next to nothing.
 //   warps 2..9  two warpgroups; each thread owns one key row (TMEM lane) and
-//               half of the 64 query columns: P^T, dS^T, and half the epilogue
+//               half of the 64 query columns: P^T, dS^T, and half of each
+//               head's accumulator drain
 // TMEM columns: dV [0,128), dK [128,320), S^T x2 [320,448), dP^T [448,512).
 // Step i packs P^T(i) AND dS^T(i) into its own S^T buffer (P^T over the first
 // 16 of each warpgroup's 32 score columns, dS^T over the other 16), so the dP^T
@@ -57,7 +69,11 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + K_BYTES;
 constexpr int OFF_STAGE = OFF_V + V_BYTES;
 constexpr int OFF_ROWV = OFF_STAGE + NSTAGE * STAGE_BYTES;
-constexpr int OFF_BARS = OFF_ROWV + NSTAGE * 2 * ROWV_BYTES;
+// per key-row warp, a [32 rows][64 B] scratch (64-byte swizzle) through which the
+// accumulator drain turns row-per-thread data into coalesced global stores
+constexpr int SCR_BYTES = 32 * 64;
+constexpr int OFF_SCR = OFF_ROWV + NSTAGE * 2 * ROWV_BYTES;
+constexpr int OFF_BARS = OFF_SCR + 8 * SCR_BYTES;
 constexpr int SMEM_BYTES = OFF_BARS + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_S = 320, COL_DP = 448;
@@ -78,6 +94,8 @@ __device__ __forceinline__ uint32_t packed_col_ds(int k) { return 16u + 8u * k +
 struct Params {
   int* status;
   int Sq, S, n_h, q_offset, causal, skv_pad, sq_pad;
+  int G;     // heads per CTA (consecutive heads blockIdx.y * G ..)
+  int n_hg;  // head groups = n_h / G: the RoPE-key partials per key row
   int q_split, q_offset2;  // second query segment (q_split = 0: none)
   int successor;  // linear block distance to the CTA that will next run on this SM (the SM count)
   float scale, scale_log2;
@@ -91,9 +109,7 @@ struct Params {
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                          const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
-                         const __grid_constant__ CUtensorMap mdO, const __grid_constant__ CUtensorMap mdV,
-                         const __grid_constant__ CUtensorMap mdK, const __grid_constant__ CUtensorMap mdKR,
-                         const Params p) {
+                         const __grid_constant__ CUtensorMap mdO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   LAGA_TRACE_CTA_BEGIN(dkdv);
   LAGA_TRACE_POINT(dkdv, 30, 0);
@@ -111,19 +127,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // dS^T(i) can complete before the waiter has seen dS^T(i-1) (dP(i) is issued
   // before that hand-off), so ds_full alternates between two barriers too.
   auto ds_full = [bars](int i) { return (i & 1) ? bars + 17 : bars + 12; };
-  uint64_t* acc_done = bars + 13;
+  uint64_t* acc_done = bars + 13;  // a head's last dK is done (one phase per head)
   uint64_t* drain = bars + 14;
   uint64_t* dp_free = bars + 16;   // dP^T(i) read into registers: dP(i+1) may overwrite it
-  // epilogue box k (16 KB) staged in shared memory; the waiter stores each as soon
-  // as it is complete, so the boxes' read-out overlaps the staging of the next
-  auto box_full = [bars](int k) { return bars + 19 + k; };
+  uint64_t* kv_empty = bars + 18;  // a head's last dP^T is done: the next head's K_nope, V may load
+  uint64_t* acc_free = bars + 19;  // dV and dK_nope drained (and dK_nope zeroed) for the next head
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kv0 = blockIdx.x * BKV;  // low key tiles see the most queries: launched first
-  const int h = blockIdx.y;
+  const int hg = blockIdx.y;         // head group: heads hg * G .. hg * G + G - 1
+  const int G = p.G;
   const int b = blockIdx.z;
   // The query tiles that see this key tile: a suffix of each segment's tiles,
   // walked segment 0 first. Step i of the walk is query tile qtile(i).
@@ -152,7 +168,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(dp_free, SOFTMAX_WARPS);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    for (int k = 0; k < 6; ++k) mbar_init(box_full(k), k == 2 ? SOFTMAX_WARPS : SOFTMAX_WARPS / 2);
+    mbar_init(kv_empty, 1);
+    mbar_init(acc_free, SOFTMAX_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,18 +185,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // Issue order: what the first MMAs need (the key/value tile, then the first
-      // query stages), and only then the successor's L2 prefetches. Each TMA
-      // instruction takes the issuing thread a while, and S(0) waits on all of
-      // the ones ahead of its tiles.
+      // query stages), and only then L2 prefetches. Each TMA instruction takes the
+      // issuing thread a while, and S(0) waits on all of the ones ahead of its tiles.
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
-      mbar_arrive_expect_tx(kv_full, K_BYTES + V_BYTES);
       const int krow = b * p.skv_pad + kv0;
-      tma_load_2d(smem + OFF_K, &mK, kv_full, h * 128, krow);
-      tma_load_2d(smem + OFF_K + KBOX, &mK, kv_full, h * 128 + 64, krow);
-      tma_load_3d(smem + OFF_K + 2 * KBOX, &mR, kv_full, 0, kv0, b);
-      tma_load_2d(smem + OFF_V, &mV, kv_full, h * 128, krow);
-      tma_load_2d(smem + OFF_V + KBOX, &mV, kv_full, h * 128 + 64, krow);
       // Warm L2 with the first tiles of the CTA that will run next on this SM
       // (about one CTA lifetime from now): its start then waits on L2, not HBM.
       auto prefetch_successor = [&]() {
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const long long nb = blockIdx.x + nx * (blockIdx.y + ny * blockIdx.z) + p.successor;
         if (nb < nx * ny * gridDim.z) {
           const int nkv0 = static_cast<int>(nb % nx) * BKV;
-          const int nh = static_cast<int>((nb / nx) % ny);
+          const int nh = static_cast<int>((nb / nx) % ny) * G;
           const int nbb = static_cast<int>(nb / (nx * ny));
           const int nrow = nbb * p.skv_pad + nkv0;
           tma_prefetch_2d(&mK, nh * 128, nrow);
@@ -205,71 +215,87 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       };
-      int i = 0;
-      for (; i < n_qt; ++i) {
-        const int s = i % NSTAGE;
-        if (!mbar_wait_or_abort(&q_empty[s], ((i / NSTAGE) & 1) ^ 1, abort_flag, 51)) break;
-        LAGA_TRACE_POINT(dkdv, 20, i);
-        const int q0 = qtile(i) * BQ;
-        uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
-        float* rows = reinterpret_cast<float*>(smem + OFF_ROWV) + s * 2 * BQ;
-        mbar_arrive_expect_tx(&q_full[s], STAGE_BYTES + 2 * ROWV_BYTES);
-        tma_load_3d(st, &mQ, &q_full[s], h * 192, q0, b);
-        tma_load_3d(st + QBOX, &mQ, &q_full[s], h * 192 + 64, q0, b);
-        tma_load_3d(st + 2 * QBOX, &mQ, &q_full[s], h * 192 + 128, q0, b);
-        tma_load_3d(st + Q_BYTES, &mdO, &q_full[s], h * 128, q0, b);
-        tma_load_3d(st + Q_BYTES + QBOX, &mdO, &q_full[s], h * 128 + 64, q0, b);
-        const long long roff = (static_cast<long long>(b) * p.n_h + h) * p.sq_pad + q0;
-        bulk_load(rows, p.lse2 + roff, ROWV_BYTES, &q_full[s]);
-        bulk_load(rows + BQ, p.delta + roff, ROWV_BYTES, &q_full[s]);
-        if (i == NSTAGE - 1 || (i == n_qt - 1 && n_qt < NSTAGE)) prefetch_successor();
+      bool ok = true;
+      int gs = 0;  // global step: head u's step i is u * n_qt + i (stage ring, barrier phases)
+      int kv_loads = 0;
+      for (int u = 0; u < G && ok; ++u) {
+        const int h = hg * G + u;
+        if (u > 0 && !mbar_wait_or_abort(kv_empty, (u - 1) & 1, abort_flag, 57)) {
+          ok = false;
+          break;
+        }
+        // head u's K_nope and V over the previous head's; the RoPE key tile is shared
+        mbar_arrive_expect_tx(kv_full, (u == 0 ? K_BYTES : 2 * KBOX) + V_BYTES);
+        tma_load_2d(smem + OFF_K, &mK, kv_full, h * 128, krow);
+        tma_load_2d(smem + OFF_K + KBOX, &mK, kv_full, h * 128 + 64, krow);
+        if (u == 0) tma_load_3d(smem + OFF_K + 2 * KBOX, &mR, kv_full, 0, kv0, b);
+        tma_load_2d(smem + OFF_V, &mV, kv_full, h * 128, krow);
+        tma_load_2d(smem + OFF_V + KBOX, &mV, kv_full, h * 128 + 64, krow);
+        ++kv_loads;
+        for (int i = 0; i < n_qt; ++i, ++gs) {
+          if (u + 1 < G && i == max(0, n_qt - 4)) {
+            // the next head's key/value tile, into L2 a few steps before the boundary load
+            tma_prefetch_2d(&mK, (h + 1) * 128, krow);
+            tma_prefetch_2d(&mK, (h + 1) * 128 + 64, krow);
+            tma_prefetch_2d(&mV, (h + 1) * 128, krow);
+            tma_prefetch_2d(&mV, (h + 1) * 128 + 64, krow);
+          }
+          const int s = gs % NSTAGE;
+          if (!mbar_wait_or_abort(&q_empty[s], ((gs / NSTAGE) & 1) ^ 1, abort_flag, 51)) {
+            ok = false;
+            break;
+          }
+          LAGA_TRACE_POINT(dkdv, 20, gs);
+          const int q0 = qtile(i) * BQ;
+          uint8_t* st = smem + OFF_STAGE + s * STAGE_BYTES;
+          float* rows = reinterpret_cast<float*>(smem + OFF_ROWV) + s * 2 * BQ;
+          mbar_arrive_expect_tx(&q_full[s], STAGE_BYTES + 2 * ROWV_BYTES);
+          tma_load_3d(st, &mQ, &q_full[s], h * 192, q0, b);
+          tma_load_3d(st + QBOX, &mQ, &q_full[s], h * 192 + 64, q0, b);
+          tma_load_3d(st + 2 * QBOX, &mQ, &q_full[s], h * 192 + 128, q0, b);
+          tma_load_3d(st + Q_BYTES, &mdO, &q_full[s], h * 128, q0, b);
+          tma_load_3d(st + Q_BYTES + QBOX, &mdO, &q_full[s], h * 128 + 64, q0, b);
+          const long long roff = (static_cast<long long>(b) * p.n_h + h) * p.sq_pad + q0;
+          bulk_load(rows, p.lse2 + roff, ROWV_BYTES, &q_full[s]);
+          bulk_load(rows + BQ, p.delta + roff, ROWV_BYTES, &q_full[s]);
+          if (u == 0 && (i == NSTAGE - 1 || (i == n_qt - 1 && n_qt < NSTAGE))) prefetch_successor();
+        }
       }
       if (n_qt <= 0) prefetch_successor();
-      if (i < n_qt) {
-        mbar_drain(kv_full, 0);
-        for (int k = i - NSTAGE < 0 ? 0 : i - NSTAGE; k < i; ++k)
+      if (!ok) {
+        // let copies already in flight land before shared memory goes away
+        if (kv_loads > 0) mbar_drain(kv_full, (kv_loads - 1) & 1);
+        for (int k = gs - NSTAGE < 0 ? 0 : gs - NSTAGE; k < gs; ++k)
           mbar_drain(&q_full[k % NSTAGE], (k / NSTAGE) & 1);
       }
     }
   } else if (warp == WAITER_WARP) {
-    // The waiter walks the MMA warp's waits in the same order: kv_full, then per
-    // step i p_full(i), dp_free(i) (i + 1 < n), ds_full(i) (i >= 0) and q_full(i+2)
+    // The waiter walks the MMA warp's waits in the same order: per head u kv_full,
+    // then per step (global index gs = u * n_qt + i) p_full(gs) (with, at a head's
+    // first step after the first head, acc_free: the previous head's accumulators
+    // drained), dp_free(gs) (i + 1 < n), ds_full(gs) (i >= 0) and q_full(gs+2)
     // (i + 2 < n). Each wait ends at the named barrier; a failed wait (timeout or
     // abort) is ANDed in, and both warps leave their loops at the same hand-off.
-    auto handoff = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
-      const bool w = warp_wait_or_abort(bar, parity, abort_flag, where);
-      return bar_and(HANDOFF_BAR, 64, w);
+    auto handoff = [&](bool w) -> bool { return bar_and(HANDOFF_BAR, 64, w); };
+    auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+      return warp_wait_or_abort(bar, parity, abort_flag, where);
     };
-    bool all_ok = handoff(kv_full, 0, 52);
-    if (all_ok) {
+    bool all_ok = true;
+    for (int u = 0; u < G && all_ok; ++u) {
+      if (!handoff(wait(kv_full, u & 1, 52))) { all_ok = false; break; }
       for (int i = -2; i < n_qt; ++i) {
+        const int gs = u * n_qt + i;
         if (i >= 0) {
-          if (!handoff(&p_full[i & 1], (i >> 1) & 1, 54)) { all_ok = false; break; }
-          if (i + 1 < n_qt && !handoff(dp_free, i & 1, 56)) { all_ok = false; break; }
-          if (!handoff(ds_full(i), (i >> 1) & 1, 55)) { all_ok = false; break; }
+          const bool freed = (i == 0 && u > 0) ? wait(acc_free, (u - 1) & 1, 58) : true;
+          if (!handoff(freed && wait(&p_full[gs & 1], (gs >> 1) & 1, 54))) { all_ok = false; break; }
+          if (i + 1 < n_qt && !handoff(wait(dp_free, gs & 1, 56))) { all_ok = false; break; }
+          if (!handoff(wait(ds_full(gs), (gs >> 1) & 1, 55))) { all_ok = false; break; }
         }
-        if (i + 2 < n_qt && !handoff(&q_full[(i + 2) % NSTAGE], ((i + 2) / NSTAGE) & 1, 53)) {
+        if (i + 2 < n_qt && !handoff(wait(&q_full[(gs + 2) % NSTAGE], ((gs + 2) / NSTAGE) & 1, 53))) {
           all_ok = false;
           break;
         }
       }
-    }
-    // Epilogue stores, one 16 KB box at a time in the order the boxes complete
-    // (warpgroup 0 stages boxes 0, 1 and half of 2; warpgroup 1 boxes 3, 4, 5 and
-    // the other half of 2). The tensor-map store reads a box out of shared memory
-    // at ~28 B/clk; issued box by box, that overlaps the staging of the others.
-    if (all_ok && lane == 0) {
-      const int row = b * p.skv_pad + kv0;
-      for (int j = 0; j < 6; ++j) {
-        const int k = j == 0 ? 0 : j == 1 ? 3 : j == 2 ? 1 : j == 3 ? 4 : j == 4 ? 5 : 2;
-        if (!mbar_wait_or_abort(box_full(k), 0, abort_flag, 65)) break;
-        uint8_t* box = smem + OFF_STAGE + k * 16384;
-        if (k < 2) tma_store_2d(&mdV, box, h * 128 + 64 * k, row);
-        else if (k < 4) tma_store_2d(&mdK, box, h * 128 + 64 * (k - 2), row);
-        else tma_store_2d(&mdKR, box, h * 64 + 32 * (k - 4), row);
-        bulk_commit_group();
-      }
-      bulk_wait_read_all();  // the staging memory is read out; the writes finish on their own
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -281,7 +307,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       return r;
     };
-    bool ok = ready();  // key/value tile
+    bool ok = true;
     bool issued = false;
     const uint64_t k_desc = sdesc_sw128(smem_u32(smem + OFF_K), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
@@ -311,7 +337,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // One loop issues everything, the first steps included, so that every MMA
     // group exists once in the binary: code run once per CTA falls out of the
     // instruction cache between CTAs and then issues several times slower.
-    // Iteration i: dV(i) (i >= 0); dP(i+1) (0 <= i+1 < n); dK(i) (i >= 0); S(i+2) (i+2 < n).
+    // Per head u, iteration i: dV(i) (i >= 0); dP(i+1) (0 <= i+1 < n); dK(i)
+    // (i >= 0); S(i+2) (i+2 < n). Steps are numbered globally (gs = u * n_qt + i)
+    // for the stage ring, the S^T buffers and the barrier phases.
 #ifdef LAGA_TRACE
     // trace build only: cycles spent at each hand-off
     long long st_cyc[3] = {0, 0, 0};
@@ -322,44 +350,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #define DKDV_STAT_BEGIN(k)
 #define DKDV_STAT_END(k)
 #endif
-    for (int i = -2; i < n_qt && ok; ++i) {
-      if (i >= 0) {
-        DKDV_STAT_BEGIN(0)
-        if (!ready()) { ok = false; break; }  // P^T(i)
-        DKDV_STAT_END(0)
-        if (lane == 0) LAGA_TRACE_POINT(dkdv, 5, i);
-        // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
-        const uint64_t do_mn = stage_desc(i, Q_BYTES, QBOX);
-        const uint32_t pt = tmem + COL_S + 64u * (i & 1);
-        mma4_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), pt + packed_col(2), pt + packed_col(3),
-                     do_mn, do_mn + (2048 >> 4), do_mn + (4096 >> 4), do_mn + (6144 >> 4), IDESC_DV,
-                     i > 0 ? 1u : 0u);
-        if (i + 1 < n_qt) {
-          if (!ready()) { ok = false; break; }  // dP^T(i) read out: dP(i+1) may overwrite it
-          issue_dp(i + 1);
+    for (int u = 0; u < G && ok; ++u) {
+      if (!ready()) { ok = false; break; }  // head u's key/value tile
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 4, u);
+      for (int i = -2; i < n_qt; ++i) {
+        const int gs = u * n_qt + i;
+        if (i >= 0) {
+          DKDV_STAT_BEGIN(0)
+          if (!ready()) { ok = false; break; }  // P^T(i) (and, at i = 0 after the first head, acc_free)
+          DKDV_STAT_END(0)
+          if (lane == 0) LAGA_TRACE_POINT(dkdv, 5, gs);
+          // dV += P^T dO_i : A = P^T (TMEM, packed bf16), B = dO_i read MN-major
+          const uint64_t do_mn = stage_desc(gs, Q_BYTES, QBOX);
+          const uint32_t pt = tmem + COL_S + 64u * (gs & 1);
+          mma4_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), pt + packed_col(2),
+                       pt + packed_col(3), do_mn, do_mn + (2048 >> 4), do_mn + (4096 >> 4), do_mn + (6144 >> 4),
+                       IDESC_DV, i > 0 ? 1u : 0u);
+          if (i + 1 < n_qt) {
+            if (!ready()) { ok = false; break; }  // dP^T(i) read out: dP(i+1) may overwrite it
+            issue_dp(gs + 1);
+            if (i + 2 == n_qt) mma_commit_warp(kv_empty);  // head u's last reader of K and V
+          }
+          DKDV_STAT_BEGIN(1)
+          if (!ready()) { ok = false; break; }  // dS^T(i)
+          DKDV_STAT_END(1)
+          if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, gs);
+          // dK += dS^T Q_i : all 192 head dims in one product; dS^T(i) sits in S^T(i)'s
+          // buffer. From the second head on dK_nope starts zeroed and the RoPE-key
+          // columns carry the previous heads' sum, so every product accumulates.
+          const uint64_t q_mn = stage_desc(gs, 0, QBOX);
+          mma4_ts_warp(tmem + COL_DK, pt + packed_col_ds(0), pt + packed_col_ds(1), pt + packed_col_ds(2),
+                       pt + packed_col_ds(3), q_mn, q_mn + (2048 >> 4), q_mn + (4096 >> 4), q_mn + (6144 >> 4),
+                       IDESC_DK, (i > 0 || u > 0) ? 1u : 0u);
+          mma_commit_warp(&q_empty[gs % NSTAGE]);
+        } else if (i + 1 == 0 && n_qt > 0) {
+          issue_dp(gs + 1);  // its stage was handed over before S(0)
+          if (n_qt == 1) mma_commit_warp(kv_empty);
         }
-        DKDV_STAT_BEGIN(1)
-        if (!ready()) { ok = false; break; }  // dS^T(i)
-        DKDV_STAT_END(1)
-        if (lane == 0) LAGA_TRACE_POINT(dkdv, 6, i);
-        // dK += dS^T Q_i : all 192 head dims in one product; dS^T(i) sits in S^T(i)'s buffer
-        const uint64_t q_mn = stage_desc(i, 0, QBOX);
-        mma4_ts_warp(tmem + COL_DK, pt + packed_col_ds(0), pt + packed_col_ds(1), pt + packed_col_ds(2),
-                     pt + packed_col_ds(3), q_mn, q_mn + (2048 >> 4), q_mn + (4096 >> 4), q_mn + (6144 >> 4),
-                     IDESC_DK, i > 0 ? 1u : 0u);
-        mma_commit_warp(&q_empty[i % NSTAGE]);
-      } else if (i + 1 == 0 && n_qt > 0) {
-        issue_dp(0);  // its stage was handed over before S(0)
+        if (i + 2 < n_qt) {
+          DKDV_STAT_BEGIN(2)
+          if (!ready()) { ok = false; break; }  // Q_{i+2}, dO_{i+2}, lse and D rows
+          DKDV_STAT_END(2)
+          if (lane == 0) LAGA_TRACE_POINT(dkdv, 7, gs + 2);
+          issue_s(gs + 2);
+          issued = true;
+          if (lane == 0) LAGA_TRACE_POINT(dkdv, 8, gs + 2);
+        }
       }
-      if (i + 2 < n_qt) {
-        DKDV_STAT_BEGIN(2)
-        if (!ready()) { ok = false; break; }  // Q_{i+2}, dO_{i+2}, lse and D rows
-        DKDV_STAT_END(2)
-        if (lane == 0) LAGA_TRACE_POINT(dkdv, 7, i + 2);
-        issue_s(i + 2);
-        issued = true;
-        if (lane == 0) LAGA_TRACE_POINT(dkdv, 8, i + 2);
-      }
+      if (!ok) break;
+      if (n_qt <= 0) mma_commit_warp(kv_empty);  // no MMA read the tile
+      mma_commit_warp(acc_done);  // head u's accumulators are final
     }
 #ifdef LAGA_TRACE
     if (lane == 0) {
@@ -368,14 +408,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         LAGA_TRACE_STAT(dkdv, 3 + k, st_cyc[k]);
       }
       LAGA_TRACE_STAT(dkdv, 6, clock64() - st_t0);
-      LAGA_TRACE_STAT(dkdv, 7, n_qt);
+      LAGA_TRACE_STAT(dkdv, 7, G * n_qt);
     }
 #endif
 #undef DKDV_STAT_BEGIN
 #undef DKDV_STAT_END
-    if (ok) {
-      mma_commit_warp(acc_done);
-    } else if (issued) {
+    if (!ok && issued) {
       mma_commit_warp(drain);
       if (lane == 0) mbar_drain(drain, 0);
       __syncwarp();
@@ -398,136 +436,165 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();  // order lane 0's acquire before the other lanes' reads
       return all;
     };
-    for (int i = 0; i < n_qt; ++i) {
-      const int s = i % NSTAGE;
-      const int qt = qtile(i);
-      const int qc = qt * BQ + 32 * half;  // this thread's first query column
-      const int q_min = qt < seg_tiles ? q_min0 : q_min1;
-      if (!warp_wait(&q_full[s], (i / NSTAGE) & 1, 61)) { ok = false; break; }
-      if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, 62)) { ok = false; break; }
-      if (lane == 0) LAGA_TRACE_POINT(dkdv, 10, i);
-      tc_fence_after();
-      // this half-tile's 32 lse and D values (16-byte aligned rows in shared memory)
-      const float4* lse4 = reinterpret_cast<const float4*>(smem + OFF_ROWV) + (s * 2 * BQ + 32 * half) / 4;
-      float lse[32], dlt[32];
+    // Accumulator drain, straight from TMEM to global memory (the stage ring is busy
+    // with the next head's tiles): warpgroup `half` moves dV and dK_nope columns
+    // [64*half, 64*half + 64) of its 32 rows as bf16 (dK scaled by the softmax
+    // scale) and, after the group's last head, the RoPE-key columns [32*half,
+    // 32*half + 32) (fp32, this head group's partial). After each head's steps its
+    // accumulators are moved out, dK_nope is zeroed and both are released
+    // (acc_free) for the next head's first dV and dK, while the tensor pipe runs
+    // the next head's first S^T and dP^T. A 32-column chunk of the warp's 32 rows
+    // goes TMEM -> registers -> the warp's scratch (row-per-thread) -> global
+    // memory as 4 stores of 8 rows x 64 contiguous bytes (row-per-thread global
+    // stores touch 32 lines per instruction and made a drain ~6K cycles long).
+    uint8_t* scr = smem + OFF_SCR + (warp - 2) * SCR_BYTES;
+    const long long row0 = static_cast<long long>(b) * p.skv_pad + kv0 + quarter * 32;  // the warp's first row
+    auto put_chunk = [&](const uint32_t (&w)[16], auto&& dst_of_row) {
+      __syncwarp();  // the previous chunk's scratch reads are done
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 a = lse4[k], d = lse4[k + BQ / 4];
-        lse[4 * k + 0] = a.x;
-        lse[4 * k + 1] = a.y;
-        lse[4 * k + 2] = a.z;
-        lse[4 * k + 3] = a.w;
-        dlt[4 * k + 0] = d.x;
-        dlt[4 * k + 1] = d.y;
-        dlt[4 * k + 2] = d.z;
-        dlt[4 * k + 3] = d.w;
-      }
-      const uint32_t s_addr = tmem + COL_S + 64u * (i & 1) + lane_off;
-      float pr[32];
-      {
-        uint32_t u[32];
-        tmem_ld32(s_addr + 32 * half, u);
-        tmem_wait_ld();
-        if (qc >= q_min) {  // every query of the half-tile sees this key
-#pragma unroll
-          for (int k = 0; k < 32; ++k) pr[k] = ex2_approx(fmaf(__uint_as_float(u[k]), p.scale_log2, -lse[k]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            pr[k] = qc + k >= q_min ? ex2_approx(fmaf(__uint_as_float(u[k]), p.scale_log2, -lse[k])) : 0.f;
-        }
-      }
-      {
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
-        // P^T packed in place over this half's own score columns (query pair k -> column
-        // 32*half + k), so the other warpgroup's scores are never overwritten unread
-        tmem_st16(s_addr + 32 * half, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
+      for (int q4 = 0; q4 < 4; ++q4)
+        *reinterpret_cast<uint4*>(scr + sw64_offset(lane, q4)) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[i & 1]);
-      if (lane == 0) LAGA_TRACE_POINT(dkdv, 11, i);
-      if (!warp_wait(dp_full, i & 1, 63)) { ok = false; break; }
-      if (lane == 0) LAGA_TRACE_POINT(dkdv, 12, i);
-      tc_fence_after();
-      const uint32_t dp_addr = tmem + COL_DP + lane_off;
-      {
-        uint32_t u[32];
-        tmem_ld32(dp_addr + 32 * half, u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = 8 * k + (lane >> 2), ch = lane & 3;
+        *reinterpret_cast<uint4*>(dst_of_row(row0 + rr) + 16 * ch) =
+            *reinterpret_cast<const uint4*>(scr + sw64_offset(rr, ch));
+      }
+    };
+    const bool z = n_qt <= 0;  // no query sees this key tile: the accumulators were never written
+    auto drain = [&](int hh, bool is_dk) {  // head hh's dV (or dK_nope) columns of this warpgroup
+#pragma unroll 1
+      for (int j = 0; j < 2; ++j) {
+        const int c = 2 * half + j;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + (is_dk ? COL_DK : COL_DV) + 32 * c, v);
         tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dp_free);  // dP(i+1) may overwrite the dP^T columns
+        const float sc = is_dk ? p.scale : 1.f;
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          w[k] = pack_bf16x2(pr[2 * k] * (__uint_as_float(u[2 * k]) - dlt[2 * k]),
-                             pr[2 * k + 1] * (__uint_as_float(u[2 * k + 1]) - dlt[2 * k + 1]));
-        // dS^T packed over this half's second 16 score columns of S^T(i) (already read)
-        tmem_st16(s_addr + 32 * half + 16, w);
+          w[k] = z ? 0u : pack_bf16x2(__uint_as_float(v[2 * k]) * sc, __uint_as_float(v[2 * k + 1]) * sc);
+        bf16* base = is_dk ? p.dk_ws : p.dv_ws;
+        put_chunk(w, [&](long long row) {
+          return reinterpret_cast<uint8_t*>(base + (row * p.n_h + hh) * 128 + 32 * c);
+        });
       }
-      tmem_wait_st();
+    };
+    auto release = [&](uint64_t* bar) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full(i));
-      if (lane == 0) LAGA_TRACE_POINT(dkdv, 13, i);
-    }
-    if (ok && warp_wait(acc_done, 0, 64)) {
-      LAGA_TRACE_POINT(dkdv, 29, 0);
-      tc_fence_after();
-      // Every MMA is done, so the Q/dO stage ring is free: stage the tiles there
-      // in the 128-byte-swizzled box layout and write them with tensor-map stores.
-      // Boxes (16 KB each): 0,1 dV columns [0,64),[64,128); 2,3 dK_nope; 4,5 this
-      // head's RoPE-key gradient (fp32) columns [0,32),[32,64).
-      // TMEM columns: dV 0..127, dK 128..319 (no-RoPE 128..255, RoPE 256..319);
-      // warpgroup 0 reads chunks 0..4, warpgroup 1 chunks 5..9 (32 columns each)
-      uint8_t* stg = smem + OFF_STAGE;
-      // warpgroup 0: chunks 0, 1 (box 0), 2, 3 (box 1), 4 (box 2);
-      // warpgroup 1: chunks 6, 7 (box 3), 8 (box 4), 9 (box 5), 5 (box 2)
-#pragma unroll 1
-      for (int j = 0; j < 5; ++j) {
-        const int c = half == 0 ? j : (j < 4 ? 6 + j : 5);
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + c * 32, u);
-        tmem_wait_ld();
-        if (n_qt <= 0) {  // no query sees this key tile: the accumulators were never written
+      if (lane == 0) mbar_arrive(bar);
+    };
+    for (int u = 0; u < G && ok; ++u) {
+      const int h = hg * G + u;
+      for (int i = 0; i < n_qt; ++i) {
+        const int gs = u * n_qt + i;
+        const int s = gs % NSTAGE;
+        const int qt = qtile(i);
+        const int qc = qt * BQ + 32 * half;  // this thread's first query column
+        const int q_min = qt < seg_tiles ? q_min0 : q_min1;
+        if (!warp_wait(&q_full[s], (gs / NSTAGE) & 1, 61)) { ok = false; break; }
+        if (!warp_wait(&s_full[gs & 1], (gs >> 1) & 1, 62)) { ok = false; break; }
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 10, gs);
+        tc_fence_after();
+        // this half-tile's 32 lse and D values (16-byte aligned rows in shared memory)
+        const float4* lse4 = reinterpret_cast<const float4*>(smem + OFF_ROWV) + (s * 2 * BQ + 32 * half) / 4;
+        float lse[32], dlt[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) u[k] = 0u;
+        for (int k = 0; k < 8; ++k) {
+          const float4 a = lse4[k], d = lse4[k + BQ / 4];
+          lse[4 * k + 0] = a.x;
+          lse[4 * k + 1] = a.y;
+          lse[4 * k + 2] = a.z;
+          lse[4 * k + 3] = a.w;
+          dlt[4 * k + 0] = d.x;
+          dlt[4 * k + 1] = d.y;
+          dlt[4 * k + 2] = d.z;
+          dlt[4 * k + 3] = d.w;
         }
-        int done_box = -1;  // the box this chunk completes (for this warpgroup)
-        if (c < 8) {
-          const float sc = c < 4 ? 1.f : p.scale;
-          uint8_t* box = stg + (c >> 1) * 16384;
+        const uint32_t s_addr = tmem + COL_S + 64u * (gs & 1) + lane_off;
+        float pr[32];
+        {
+          uint32_t u[32];
+          tmem_ld32(s_addr + 32 * half, u);
+          tmem_wait_ld();
+          if (qc >= q_min) {  // every query of the half-tile sees this key
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * sc, __uint_as_float(u[8 * v + 1]) * sc);
-            w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * sc, __uint_as_float(u[8 * v + 3]) * sc);
-            w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * sc, __uint_as_float(u[8 * v + 5]) * sc);
-            w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * sc, __uint_as_float(u[8 * v + 7]) * sc);
-            *reinterpret_cast<uint4*>(box + sw128_offset(r, (c & 1) * 4 + v)) = w;
-          }
-          if ((c & 1) == 1 || c == 4) done_box = c >> 1;  // chunk 5 completes box 2 for warpgroup 1
-        } else {
-          uint8_t* box = stg + (4 + c - 8) * 16384;
+            for (int k = 0; k < 32; ++k) pr[k] = ex2_approx(fmaf(__uint_as_float(u[k]), p.scale_log2, -lse[k]));
+          } else {
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            uint4 w;
-            w.x = __float_as_uint(__uint_as_float(u[4 * v + 0]) * p.scale);
-            w.y = __float_as_uint(__uint_as_float(u[4 * v + 1]) * p.scale);
-            w.z = __float_as_uint(__uint_as_float(u[4 * v + 2]) * p.scale);
-            w.w = __float_as_uint(__uint_as_float(u[4 * v + 3]) * p.scale);
-            *reinterpret_cast<uint4*>(box + sw128_offset(r, v)) = w;
+            for (int k = 0; k < 32; ++k)
+              pr[k] = qc + k >= q_min ? ex2_approx(fmaf(__uint_as_float(u[k]), p.scale_log2, -lse[k])) : 0.f;
           }
-          done_box = 4 + c - 8;
         }
-        if (done_box >= 0) {
-          fence_proxy_async_smem();
+        {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+          // P^T packed in place over this half's own score columns (query pair k -> column
+          // 32*half + k), so the other warpgroup's scores are never overwritten unread
+          tmem_st16(s_addr + 32 * half, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[gs & 1]);
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 11, gs);
+        if (!warp_wait(dp_full, gs & 1, 63)) { ok = false; break; }
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 12, gs);
+        tc_fence_after();
+        const uint32_t dp_addr = tmem + COL_DP + lane_off;
+        {
+          uint32_t u[32];
+          tmem_ld32(dp_addr + 32 * half, u);
+          tmem_wait_ld();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(box_full(done_box));
+          if (lane == 0) mbar_arrive(dp_free);  // dP(i+1) may overwrite the dP^T columns
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_bf16x2(pr[2 * k] * (__uint_as_float(u[2 * k]) - dlt[2 * k]),
+                               pr[2 * k + 1] * (__uint_as_float(u[2 * k + 1]) - dlt[2 * k + 1]));
+          // dS^T packed over this half's second 16 score columns of S^T(i) (already read)
+          tmem_st16(s_addr + 32 * half + 16, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full(gs));
+        if (lane == 0) LAGA_TRACE_POINT(dkdv, 13, gs);
+      }
+      if (!ok || !warp_wait(acc_done, u & 1, 64)) { ok = false; break; }
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 29, u);
+      tc_fence_after();
+      drain(h, false);
+      drain(h, true);
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 27, u);
+      if (u + 1 < G) {
+        // dK_nope restarts from zero for the next head (its first dK accumulates)
+        uint32_t zero[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) zero[k] = 0u;
+        tmem_st32(tmem + lane_off + COL_DK + 32 * (2 * half), zero);
+        tmem_st32(tmem + lane_off + COL_DK + 32 * (2 * half + 1), zero);
+        tmem_wait_st();
+        release(acc_free);
+      } else {
+        // the RoPE-key gradient summed over this group's heads: fp32 partial hg,
+        // columns [32*half, 32*half + 32) as two 16-column (64-byte) chunks
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + COL_DK + 128 + 32 * half, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) w[k] = z ? 0u : __float_as_uint(__uint_as_float(v[16 * hh + k]) * p.scale);
+          put_chunk(w, [&](long long row) {
+            return reinterpret_cast<uint8_t*>(p.dkr_ws + (row * p.n_hg + hg) * 64 + 32 * half + 16 * hh);
+          });
         }
       }
     }
@@ -584,25 +651,6 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
     r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
-  CUtensorMap mdV, mdK, mdKR;  // epilogue stores
-  if (r.cu == CUDA_SUCCESS) {
-    const uint64_t dims[2] = {kv_inner, kv_rows};
-    const uint64_t strides[1] = {kv_inner * 2};
-    const uint32_t box[2] = {64, BKV};
-    r.cu = make_tmap(&mdV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.dv_ws, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-    if (r.cu == CUDA_SUCCESS)
-      r.cu = make_tmap(&mdK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.dk_ws, dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
-  }
-  if (r.cu == CUDA_SUCCESS) {
-    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 64;
-    const uint64_t dims[2] = {inner, kv_rows};
-    const uint64_t strides[1] = {inner * 4};
-    const uint32_t box[2] = {32, BKV};
-    r.cu = make_tmap(&mdKR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w.dkr_ws, dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  }
   if (r.cu != CUDA_SUCCESS) {
     r.what = "tensor maps attention backward (dK, dV)";
     return r;
@@ -625,13 +673,15 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
   p.dk_ws = w.dk_ws;
   p.dv_ws = w.dv_ws;
   p.dkr_ws = w.dkr_ws;
+  p.G = dkdv_heads_per_cta(d.n_h);
+  p.n_hg = d.n_h / p.G;
   p.successor = sm_count();
   r.err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (r.err != cudaSuccess) {
     r.what = "cudaFuncSetAttribute(attn_bwd_dkdv)";
     return r;
   }
-  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, mdV, mdK, mdKR, p);
+  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, p.n_hg, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_bwd_dkdv_kernel launch";
   return r;

@@ -1,14 +1,16 @@
 // Workspace layout and the small memory-bound kernels around the tensor-core
 // attention backward:
 //   pre   D_i = dout_i . out_i and lse in the log2 domain, padded per (b, h) row
-//   post  dk_rope = sum over heads of the per-head RoPE-key gradients (the RoPE
-//         key is one tensor shared by every head, so its gradient collects all
-//         of them)
+//   post  dk_rope = sum of the RoPE-key gradient partials, one per head group of
+//         the dK/dV kernel (the RoPE key is one tensor shared by every head, so its
+//         gradient collects all of them)
 #include "internal.h"
 
 namespace laga {
 
 bool tc_supported(const Dims& d) { return d.d_c == 512 && d.d_nope == 128 && d.d_v == 128 && d.d_rope == 64; }
+
+int dkdv_heads_per_cta(int n_h) { return n_h % 4 == 0 ? 4 : (n_h % 2 == 0 ? 2 : 1); }
 
 namespace {
 size_t kv_ws_bytes(const Dims& d) { return align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 128 * 2, 256); }
@@ -18,7 +20,7 @@ size_t tc_fwd_workspace(const Dims& d) { return 2 * kv_ws_bytes(d); }
 
 size_t tc_bwd_workspace(const Dims& d) {
   const size_t kv = kv_ws_bytes(d);
-  const size_t dkr = align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 64 * 4, 256);
+  const size_t dkr = align_up(static_cast<size_t>(d.B) * d.skv_pad * (d.n_h / dkdv_heads_per_cta(d.n_h)) * 64 * 4, 256);
   const size_t rows = align_up(static_cast<size_t>(d.B) * d.n_h * d.sq_pad * 4, 256);
   return 4 * kv + dkr + 2 * rows;
 }
@@ -36,7 +38,7 @@ BwdWorkspace tc_bwd_carve(const Dims& d, void* ws) {
   w.dv_ws = reinterpret_cast<bf16*>(p);
   p += kv;
   w.dkr_ws = reinterpret_cast<float*>(p);
-  p += align_up(static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 64 * 4, 256);
+  p += align_up(static_cast<size_t>(d.B) * d.skv_pad * (d.n_h / dkdv_heads_per_cta(d.n_h)) * 64 * 4, 256);
   w.lse2 = reinterpret_cast<float*>(p);
   p += align_up(static_cast<size_t>(d.B) * d.n_h * d.sq_pad * 4, 256);
   w.delta = reinterpret_cast<float*>(p);
@@ -91,8 +93,9 @@ __global__ void bwd_pre_kernel(Dims d, const bf16* __restrict__ out, const bf16*
   }
 }
 
-// dk_rope[b, j, :] = sum_h dkr[b, j, h, :]; 16 threads x 4 columns per row.
-__global__ void rope_sum_kernel(Dims d, const float* __restrict__ dkr, bf16* __restrict__ dk_rope) {
+// dk_rope[b, j, :] = sum_g dkr[b, j, g, :] over the dK/dV kernel's head-group
+// partials; 16 threads x 4 columns per row.
+__global__ void rope_sum_kernel(Dims d, int parts, const float* __restrict__ dkr, bf16* __restrict__ dk_rope) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long total = static_cast<long long>(d.B) * d.S * 16;
   if (t >= total) return;
@@ -103,9 +106,9 @@ __global__ void rope_sum_kernel(Dims d, const float* __restrict__ dkr, bf16* __r
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (j < d.skv_pad) {
     const float4* src =
-        reinterpret_cast<const float4*>(dkr + ((static_cast<long long>(b) * d.skv_pad + j) * d.n_h) * 64) + c4;
-    for (int h = 0; h < d.n_h; ++h) {
-      const float4 v = src[h * 16];
+        reinterpret_cast<const float4*>(dkr + ((static_cast<long long>(b) * d.skv_pad + j) * parts) * 64) + c4;
+    for (int g = 0; g < parts; ++g) {
+      const float4 v = src[g * 16];
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
@@ -133,7 +136,8 @@ LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const 
 LaunchResult tc_bwd_post(const Dims& d, const BwdWorkspace& w, bf16* dk_rope, cudaStream_t st) {
   LaunchResult r;
   const long long t = static_cast<long long>(d.B) * d.S * 16;
-  rope_sum_kernel<<<static_cast<unsigned>((t + 255) / 256), 256, 0, st>>>(d, w.dkr_ws, dk_rope);
+  rope_sum_kernel<<<static_cast<unsigned>((t + 255) / 256), 256, 0, st>>>(d, d.n_h / dkdv_heads_per_cta(d.n_h),
+                                                                          w.dkr_ws, dk_rope);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "bwd post kernels";
   return r;

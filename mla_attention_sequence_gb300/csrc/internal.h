@@ -86,11 +86,14 @@ struct BwdWorkspace {
   bf16* v_ws;       // [B][skv_pad][n_h*128]
   bf16* dk_ws;      // [B][skv_pad][n_h*128]
   bf16* dv_ws;      // [B][skv_pad][n_h*128]
-  float* dkr_ws;    // [B][skv_pad][n_h][64]  per-head RoPE-key gradient
+  float* dkr_ws;    // [B][skv_pad][n_h / G][64]  RoPE-key gradient per head group (fp32)
   float* lse2;      // [B][n_h][sq_pad]  lse * log2(e), +inf on padded rows
   float* delta;     // [B][n_h][sq_pad]  rowsum(dout * out), 0 on padded rows
 };
 BwdWorkspace tc_bwd_carve(const Dims& d, void* ws);
+// Heads per dK/dV CTA (G): the CTA walks G consecutive heads of one key tile and
+// sums their RoPE-key gradients in TMEM, so the workspace holds n_h / G partials.
+int dkdv_heads_per_cta(int n_h);
 
 LaunchResult tc_bwd_pre(const Dims& d, const bf16* out, const bf16* dout, const float* lse, const BwdWorkspace& w,
                         cudaStream_t st);
