@@ -56,13 +56,14 @@ def load_peaks():
 # DRAM traffic per launch of a kernel, from one ncu capture of the kernel source
 # identified by `src_sha` (sha256 of the kernel file followed by csrc/ptx.cuh,
 # first 16 hex digits). It is reported only while the source is unchanged.
-# attn_bwd_dkdv: dram__bytes_read.sum + dram__bytes_write.sum = 634.2 + 757.3 MB
+# attn_bwd_dkdv: dram__bytes_read.sum + dram__bytes_write.sum = 740.7 + 563.0 MB
 # on the n_h = 64 last-rank shard (the full n_h = 128 shard exceeds the size rule
 # for a multi-pass capture); the kernel's work and both byte streams (K/V and
-# Q/dO tiles in, dK/dV/dK_rope out) scale with the head count, so x2.
+# Q/dO tiles in, dK/dV and the head-group RoPE-key partials out) scale with the
+# head count, so x2.
 MEASURED_TRAFFIC = {
-    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "f22ea5027c21062e",
-                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (634.227456e6 + 757.337344e6)}},
+    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "ee553712b728cd19",
+                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (740.726528e6 + 563.041536e6)}},
 }
 
 
