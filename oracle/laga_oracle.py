@@ -36,6 +36,7 @@ memory, they do not change the arithmetic.
 absorbed_forward writes out the absorbed MLA form the Abstract contrasts LAGA
 with (W_UK folded into the query, attention in the latent space); it reaches
 the same out and lse by a different factorisation of the same scores.
+absorbed_backward takes that form's gradients through its own steps.
 
 Every function here has a pin in the CPU test suite (brute-force attention,
 the absorbed form against the explicit one, sequence-parallel shard
@@ -275,6 +276,59 @@ def absorbed_forward(q, c_kv, k_rope, W_UK, W_UV, q_offset=0, causal=True, scale
         keep["ctx"] = ctx_all
     return out, lse
 
+
+
+def absorbed_backward(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset=0, causal=True, scale=None):
+    """Gradients of <dout, out> for the absorbed form, taken through its own steps
+    (the latent-space context and the absorbed query), per (batch, head):
+
+      dctx = dout W_UV_h^T,           dW_UV_h = ctx^T dout,
+      dP = dctx c_kv^T,               dS = P o (dP - rowsum(dP o P)),
+      dq_lat = scale dS c_kv,         dq_rope = scale dS k_rope,
+      dc_kv += scale dS^T q_lat + P^T dctx,   dk_rope += scale dS^T q_rope,
+      dq_nope = dq_lat W_UK_h,        dW_UK_h = dq_lat^T q_nope_h.
+
+    The absorbed form is the explicit form's function written another way, so these
+    equal mla_backward's gradients up to rounding. Returns the same dict
+    (dq, dc_kv, dk_rope, dW_UK, dW_UV), fp64."""
+    B, Sq, n_h, d_qk = q.shape
+    S, d_c = c_kv.shape[1], c_kv.shape[2]
+    d_nope = W_UK.shape[1] // n_h
+    d_v = W_UV.shape[1] // n_h
+    if scale is None:
+        scale = default_scale(d_nope, d_qk - d_nope)
+    dq = np.zeros((B, Sq, n_h, d_qk))
+    dc_kv = np.zeros((B, S, d_c))
+    dk_rope = np.zeros((B, S, d_qk - d_nope))
+    dW_UK = np.zeros((d_c, n_h * d_nope))
+    dW_UV = np.zeros((d_c, n_h * d_v))
+    for b in range(B):
+        c = _f64(c_kv[b])
+        r = _f64(k_rope[b])
+        key = np.concatenate([c, r], axis=1)
+        for h in range(n_h):
+            wk = _f64(W_UK[:, h * d_nope:(h + 1) * d_nope])
+            wv = _f64(W_UV[:, h * d_v:(h + 1) * d_v])
+            q_nope = _f64(q[b, :, h, :d_nope])
+            q_rope = _f64(q[b, :, h, d_nope:])
+            q_lat = q_nope @ wk.T
+            s = scale * (np.concatenate([q_lat, q_rope], axis=1) @ key.T)
+            s = np.where(visible_mask(np.arange(Sq), S, q_offset, causal), s, -np.inf)
+            e = np.exp(s - s.max(axis=1, keepdims=True))
+            P = e / e.sum(axis=1, keepdims=True)
+            ctx = P @ c
+            g = _f64(dout[b, :, h, :])
+            dctx = g @ wv.T
+            dW_UV[:, h * d_v:(h + 1) * d_v] += ctx.T @ g
+            dP = dctx @ c.T
+            dS = P * (dP - (dP * P).sum(axis=1, keepdims=True))
+            dq_lat = scale * (dS @ c)
+            dq[b, :, h, d_nope:] = scale * (dS @ r)
+            dc_kv[b] += scale * (dS.T @ q_lat) + P.T @ dctx
+            dk_rope[b] += scale * (dS.T @ q_rope)
+            dq[b, :, h, :d_nope] = dq_lat @ wk
+            dW_UK[:, h * d_nope:(h + 1) * d_nope] += dq_lat.T @ q_nope
+    return {"dq": dq, "dc_kv": dc_kv, "dk_rope": dk_rope, "dW_UK": dW_UK, "dW_UV": dW_UV}
 
 def reconstruct(c_kv, W_UK, W_UV, n_h):
     """Step 1 for the whole batch: K_nope [B,S,n_h,d_nope] and V [B,S,n_h,d_v]."""

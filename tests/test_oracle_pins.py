@@ -271,6 +271,51 @@ def test_finite_differences_every_input(causal, q_offset):
             assert abs(fd - flat[idx]) <= 1e-6 * max(1.0, abs(flat[idx])), (name, idx, fd, flat[idx])
 
 
+def absorbed_loss(p, x, scale=None):
+    out, _ = oracle.absorbed_forward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], p.q_offset, p.causal,
+                                     scale)
+    return float((out * x["dout"]).sum())
+
+
+def run_absorbed_bwd(p, x, scale=None):
+    return O.absorbed_backward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], x["dout"], p.q_offset,
+                                    p.causal, scale)
+
+
+@pytest.mark.parametrize("causal,q_offset", [(True, 3), (False, 0)])
+def test_absorbed_backward_finite_differences(causal, q_offset):
+    """The absorbed form's backward against central differences of its own forward
+    (loss <dout, out> through q_lat and the latent-space context), in random
+    directions of every input."""
+    p = small(B=2, Sq=6, S=10, n_h=2, q_offset=q_offset, causal=causal)
+    x = inputs64(p, seed=15)
+    g = run_absorbed_bwd(p, x)
+    grads = {"q": g["dq"], "c_kv": g["dc_kv"], "k_rope": g["dk_rope"], "W_UK": g["dW_UK"], "W_UV": g["dW_UV"]}
+    rng = np.random.default_rng(19)
+    h = 1e-6
+    for name, grad in grads.items():
+        for _ in range(3):
+            direction = rng.standard_normal(x[name].shape)
+            xp, xm = dict(x), dict(x)
+            xp[name] = x[name] + h * direction
+            xm[name] = x[name] - h * direction
+            fd = (absorbed_loss(p, xp) - absorbed_loss(p, xm)) / (2 * h)
+            an = float((grad * direction).sum())
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_absorbed_backward_equals_explicit_backward():
+    """Both forms compute one function, so their gradients agree (here also at an
+    explicit scale and with the latent wider than a head)."""
+    for scale in (None, 0.3):
+        p = small(B=2, Sq=7, S=12, n_h=3, d_c=9, q_offset=5)
+        x = inputs64(p, seed=23)
+        a = run_absorbed_bwd(p, x, scale)
+        e = run_bwd(p, x, scale)
+        for k in e:
+            np.testing.assert_allclose(a[k], e[k], rtol=1e-10, atol=1e-12, err_msg=k)
+
+
 # --------------------------------------------------------------------------- autograd
 def test_torch_autograd_float64():
     """torch's CPU autograd in float64 differentiates the explicit form independently."""
@@ -494,6 +539,25 @@ def _default_scale_nope_only(d_nope, d_rope):
     return 1.0 / np.sqrt(d_nope)
 
 
+def _absorbed_backward_rope_sign(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset=0, causal=True, scale=None):
+    # a sign error on the RoPE part of dq
+    g = _ORIG_ABS_BWD(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset, causal, scale)
+    d_nope = W_UK.shape[1] // q.shape[2]
+    g["dq"][..., d_nope:] *= -1.0
+    return g
+
+
+def _absorbed_backward_rope_key_unscaled(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset=0, causal=True, scale=None):
+    # forgets the softmax scale on the RoPE-key gradient
+    g = _ORIG_ABS_BWD(q, c_kv, k_rope, W_UK, W_UV, dout, q_offset, causal, scale)
+    s = scale if scale is not None else O.default_scale(W_UK.shape[1] // q.shape[2], q.shape[3] - W_UK.shape[1] // q.shape[2])
+    g["dk_rope"] = g["dk_rope"] / s
+    return g
+
+
+_ORIG_ABS_BWD = O.absorbed_backward
+
+
 _ORIG_BWD = O.attention_head_backward
 
 
@@ -505,6 +569,7 @@ def _pins_pass():
         lambda: test_torch_autograd_float64(),
         lambda: test_hand_worked_two_token_example(),
         lambda: test_hand_worked_example_at_the_default_scale(),
+        lambda: test_absorbed_backward_finite_differences(True, 3),
     ]
     for c in checks:
         try:
@@ -521,6 +586,8 @@ def _pins_pass():
     ("attention_head_backward", _attention_backward_sign),
     ("head_key", _head_key_transposed_rope),
     ("default_scale", _default_scale_nope_only),
+    ("absorbed_backward", _absorbed_backward_rope_sign),
+    ("absorbed_backward", _absorbed_backward_rope_key_unscaled),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, target, mutant):
     assert _pins_pass()
