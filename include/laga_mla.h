@@ -143,7 +143,16 @@ typedef struct {
  *    one, so one buffer of laga_mla_bwd_workspace_size bytes serves both
  *    calls. Keeping K/V alive between the calls is the memory profile of the
  *    explicit MLA form, which stores per-head K and V for its backward. */
-typedef enum { LAGA_FLAG_REUSE_KV = 1 } laga_flags;
+/*  LAGA_FLAG_KV_PREBUILT (laga_mla_fwd): the workspace already holds this call's
+ *    per-head K_nope and V for every latent row the forward reads, written there
+ *    by laga_mla_reconstruct_rows with the same descriptor (in any number of row
+ *    ranges, in any order, on this stream or on one ordered before it). The
+ *    forward then runs the attention alone. A sequence-parallel caller can so
+ *    rebuild each chunk of the gathered latent as soon as that chunk has
+ *    arrived, overlapping the rebuild with the rest of the gather (the Abstract's
+ *    LAGA gathers the latent and rebuilds K/V locally). Tensor-core materialize
+ *    path only (LAGA_ERR_UNSUPPORTED otherwise). */
+typedef enum { LAGA_FLAG_REUSE_KV = 1, LAGA_FLAG_KV_PREBUILT = 2 } laga_flags;
 
 /* Bytes of device workspace laga_mla_fwd / laga_mla_bwd need for this
  * problem (0 if the descriptor is invalid or unsupported). The workspace must
@@ -193,6 +202,21 @@ laga_status laga_mla_bwd(const laga_mla_desc* desc, const void* q, const void* c
  * variant are used. Errors as for laga_mla_fwd. */
 laga_status laga_mla_reconstruct(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
                                  const void* W_UV, void* k_nope, void* v, laga_stream_t stream);
+
+/* laga_mla_fwd's step 1 (the local K/V rebuild) for latent rows [row0, row0 + rows)
+ * of every batch element, into the forward workspace, for a later laga_mla_fwd
+ * with LAGA_FLAG_KV_PREBUILT and the same descriptor. The forward reads the rows
+ * of the padded visible prefix, [0, Skv_pad) with Skv_pad the last row any query
+ * sees plus one, rounded up to 128; the calls must cover it, and rows past it are
+ * ignored. row0 must be a multiple of 128 and row0 + rows either a multiple of
+ * 128 or at least Skv_pad. c_kv, W_UK, W_UV are the full device tensors of
+ * laga_mla_fwd; workspace and workspace_bytes as for laga_mla_fwd (its contents
+ * outside the rebuilt rows are left alone). Tensor-core materialize path only.
+ * Errors: LAGA_ERR_INVALID_ARG (range), LAGA_ERR_UNSUPPORTED (path),
+ * LAGA_ERR_WORKSPACE before any launch; LAGA_ERR_CUDA if the launch fails. */
+laga_status laga_mla_reconstruct_rows(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
+                                      const void* W_UV, int64_t row0, int64_t rows, void* workspace,
+                                      size_t workspace_bytes, laga_stream_t stream);
 
 /* The absorbed MLA form, forward, for comparison with the library's own path.
  * Source: the LAGA page's Abstract (weekinpapers, "A Training-Memory Regression

@@ -138,7 +138,7 @@ Path plan(const laga_mla_desc* desc, Dims* d, laga_status* st, bool for_bwd) {
     *st = fail(LAGA_ERR_INVALID_ARG, "causal shard needs q_offset2 + sq - q_split <= skv%s");
     return Path::Invalid;
   }
-  if ((x.flags & ~static_cast<int32_t>(LAGA_FLAG_REUSE_KV)) != 0) {
+  if ((x.flags & ~static_cast<int32_t>(LAGA_FLAG_REUSE_KV | LAGA_FLAG_KV_PREBUILT)) != 0) {
     *st = fail(LAGA_ERR_INVALID_ARG, "unknown bits in flags%s");
     return Path::Invalid;
   }
@@ -343,6 +343,8 @@ laga_status laga_mla_fwd(const laga_mla_desc* desc, const void* q, const void* c
     return fail(LAGA_ERR_INVALID_ARG, "k_rope must be non-null and 16-byte aligned%s");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = desc->dtype == LAGA_DTYPE_BF16;
+  if ((desc->flags & LAGA_FLAG_KV_PREBUILT) && path != Path::TensorCore)
+    return fail(LAGA_ERR_UNSUPPORTED, "LAGA_FLAG_KV_PREBUILT needs the tensor-core materialize path%s");
   if (path == Path::TensorCoreFused) {
     return from_launch(timed("attn_fwd_fused", s, [&] {
       return tc_attn_fwd_fused(d, static_cast<const bf16*>(q), static_cast<const bf16*>(c_kv),
@@ -358,14 +360,46 @@ laga_status laga_mla_fwd(const laga_mla_desc* desc, const void* q, const void* c
         timed("simt_fwd", s, [&] { return simt_fwd(d, bf, q, c_kv, k_rope, W_UK, W_UV, out, lse, workspace, s); }));
   bf16* k_ws = static_cast<bf16*>(workspace);
   bf16* v_ws = k_ws + static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 128;
-  LaunchResult r = timed("recon_fwd_gemm", s, [&] {
-    return tc_recon_fwd(d, static_cast<const bf16*>(c_kv), static_cast<const bf16*>(W_UK),
-                        static_cast<const bf16*>(W_UV), k_ws, v_ws, d.skv_pad, s);
-  });
-  if (!r.ok()) return from_launch(r);
+  if (!(desc->flags & LAGA_FLAG_KV_PREBUILT)) {
+    LaunchResult r = timed("recon_fwd_gemm", s, [&] {
+      return tc_recon_fwd(d, static_cast<const bf16*>(c_kv), static_cast<const bf16*>(W_UK),
+                          static_cast<const bf16*>(W_UV), k_ws, v_ws, d.skv_pad, s);
+    });
+    if (!r.ok()) return from_launch(r);
+  }
   return from_launch(timed("attn_fwd", s, [&] {
     return tc_attn_fwd(d, static_cast<const bf16*>(q), k_ws, v_ws, static_cast<const bf16*>(k_rope),
                        static_cast<bf16*>(out), lse, s);
+  }));
+}
+
+laga_status laga_mla_reconstruct_rows(const laga_mla_desc* desc, const void* c_kv, const void* W_UK,
+                                      const void* W_UV, int64_t row0, int64_t rows, void* workspace,
+                                      size_t workspace_bytes, laga_stream_t stream) {
+  Dims d{};
+  laga_status st;
+  const Path path = plan(desc, &d, &st, false);
+  if (path == Path::Invalid) return st;
+  if (path != Path::TensorCore)
+    return fail(LAGA_ERR_UNSUPPORTED, "laga_mla_reconstruct_rows needs the tensor-core materialize path%s");
+  const void* ptrs[] = {c_kv, W_UK, W_UV};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return fail(LAGA_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned%s");
+  if (row0 < 0 || rows <= 0 || row0 % 128 != 0 || row0 > (int64_t{1} << 40) || rows > (int64_t{1} << 40))
+    return fail(LAGA_ERR_INVALID_ARG, "row0 must be a non-negative multiple of 128 and rows positive%s");
+  const int64_t end = std::min<int64_t>(row0 + rows, d.skv_pad);
+  if (row0 >= d.skv_pad) return LAGA_OK;  // rows no query sees: nothing to rebuild
+  if (end % 128 != 0) return fail(LAGA_ERR_INVALID_ARG, "row0 + rows must be a multiple of 128 or reach Skv_pad%s");
+  const size_t need = tc_fwd_workspace(d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LAGA_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small%s");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  bf16* k_ws = static_cast<bf16*>(workspace);
+  bf16* v_ws = k_ws + static_cast<size_t>(d.B) * d.skv_pad * d.n_h * 128;
+  return from_launch(timed("recon_fwd_gemm", s, [&] {
+    return tc_recon_fwd(d, static_cast<const bf16*>(c_kv), static_cast<const bf16*>(W_UK),
+                        static_cast<const bf16*>(W_UV), k_ws, v_ws, d.skv_pad, s, static_cast<int>(row0 / 128),
+                        static_cast<int>((end - row0) / 128));
   }));
 }
 

@@ -49,6 +49,7 @@ struct GemmParams {
   int d_lat;                   // QLAT: latent width (output columns per head)
   int a_head_stride;           // QLAT / OUTPROJ: A columns between heads
   int b_head_stride;           // QLAT: B columns between heads
+  int m_first;                 // K/V rebuild: first 128-row tile (a row range of the latent)
 };
 
 // Tile order: within a batch element, bands of GROUP_M m-tiles are walked n by n
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(224, 1)
         const int key = t / p.n_tiles;
         if (key == cur) continue;
         cur = key;
-        const int b = key / p.m_tiles, m = key - b * p.m_tiles;
+        const int b = key / p.m_tiles, m = key - b * p.m_tiles + p.m_first;
         for (int i = 0; i < A_BOXES; ++i, ++boxes) {
           const int buf = boxes & 1;
           if (!mbar_wait_or_abort(&ast_empty[buf], ((boxes >> 1) & 1) ^ 1, abort_flag, 6)) {
@@ -633,7 +634,7 @@ __global__ void __launch_bounds__(224, 1)
       // every MMA through tile t is done, so the latent columns may be replaced now
       if (t + 1 < t_end && (t + 1) / p.n_tiles != key && !load_latent()) break;
       const int n = t - key * p.n_tiles;
-      const int b = key / p.m_tiles, m = key - b * p.m_tiles;
+      const int b = key / p.m_tiles, m = key - b * p.m_tiles + p.m_first;
       const bool second = n >= p.n_tiles_first;
       const int n0 = (second ? n - p.n_tiles_first : n) * TL_BN;
       epilogue_tile<TL_BN, 1, TL_EPI_BUFS>(tmem_base + TL_ACC_COL + buf * TL_BN, quarter, lane, second ? &mapO1 : &mapO0, n0,
@@ -710,7 +711,7 @@ LongKShape long_k_shape(long long tiles_256x256, bool mh2_ok) {
 }
 
 LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, const bf16* W_UV, bf16* k_ws,
-                          bf16* v_ws, int rows_pad, cudaStream_t st) {
+                          bf16* v_ws, int rows_pad, cudaStream_t st, int m_first, int m_count) {
   LaunchResult r;
   if (d.d_c != TL_DC) {  // the tensor-core path is planned only for d_c = 512
     r.err = cudaErrorInvalidValue;
@@ -752,7 +753,8 @@ LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, con
     return r;
   }
   GemmParams p{};
-  p.m_tiles = rows_pad / BM;
+  p.m_first = m_first;
+  p.m_tiles = m_count < 0 ? rows_pad / BM : m_count;
   p.n_tiles_first = static_cast<int>(N / TL_BN);  // K_nope tiles, then as many V tiles
   p.n_tiles = 2 * p.n_tiles_first;
   p.batches = d.B;

@@ -67,8 +67,10 @@ size_t tc_bwd_workspace(const Dims& d);
 
 // K_nope/V for rows [0, rows) of every batch element into [B][rows_pad][n_h*128] bf16
 // (rows_pad a multiple of 128; rows beyond S come out zero).
+// K_nope / V of latent row tiles [m_first, m_first + m_count) (128 rows each; all of
+// [0, rows_pad / 128) when m_count < 0) into the [B][rows_pad][n_h * 128] buffers.
 LaunchResult tc_recon_fwd(const Dims& d, const bf16* c_kv, const bf16* W_UK, const bf16* W_UV, bf16* k_ws,
-                          bf16* v_ws, int rows_pad, cudaStream_t st);
+                          bf16* v_ws, int rows_pad, cudaStream_t st, int m_first = 0, int m_count = -1);
 // dc_kv = dK_nope W_UK^T + dV W_UV^T (rows < S; rows >= skv_pad zeroed)
 LaunchResult tc_recon_bwd_dc(const Dims& d, const bf16* dk_ws, const bf16* dv_ws, const bf16* W_UK,
                              const bf16* W_UV, bf16* dc_kv, cudaStream_t st);

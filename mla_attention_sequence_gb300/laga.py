@@ -23,11 +23,12 @@ STATUS_NAMES = {0: "LAGA_OK", 1: "LAGA_ERR_INVALID_ARG", 2: "LAGA_ERR_UNSUPPORTE
 DTYPES = {"f32": 0, "bf16": 1}
 VARIANTS = {"auto": 0, "materialize": 1, "fused_recon": 2, "simt": 3}
 FLAG_REUSE_KV = 1
+FLAG_KV_PREBUILT = 2
 
 EXPORTS = ("laga_mla_fwd_workspace_size", "laga_mla_bwd_workspace_size", "laga_mla_fwd", "laga_mla_bwd",
            "laga_mla_reconstruct", "laga_mla_check", "laga_status_string", "laga_mla_last_error",
            "laga_mla_version", "laga_mla_selftest_timeout", "laga_mla_absorbed_fwd",
-           "laga_mla_absorbed_fwd_workspace_size")
+           "laga_mla_absorbed_fwd_workspace_size", "laga_mla_reconstruct_rows")
 
 
 class LagaDesc(ctypes.Structure):
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
     L.laga_mla_absorbed_fwd.restype = st
     L.laga_mla_reconstruct.argtypes = [pd, vp, vp, vp, vp, vp, vp]
     L.laga_mla_reconstruct.restype = st
+    L.laga_mla_reconstruct_rows.argtypes = [pd, vp, vp, vp, ctypes.c_int64, ctypes.c_int64, vp, sz, vp]
+    L.laga_mla_reconstruct_rows.restype = st
     L.laga_mla_check.argtypes = [vp]
     L.laga_mla_check.restype = st
     L.laga_mla_selftest_timeout.argtypes = [vp]
@@ -159,10 +162,16 @@ def _workspace(nbytes: int, device, given: torch.Tensor | None) -> torch.Tensor 
 
 def fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset: int = 0, causal: bool = True, softmax_scale: float | None = None,
         variant: str = "auto", workspace: torch.Tensor | None = None, out=None, lse=None, q_split: int = 0,
-        q_offset2: int = 0):
-    """laga_mla_fwd: returns (out [B,Sq,n_h,d_v], lse [B,n_h,Sq] fp32)."""
+        q_offset2: int = 0, kv_prebuilt: bool = False):
+    """laga_mla_fwd: returns (out [B,Sq,n_h,d_v], lse [B,n_h,Sq] fp32).
+
+    kv_prebuilt=True (LAGA_FLAG_KV_PREBUILT): `workspace` already holds K_nope / V
+    for every row the forward reads, from reconstruct_rows calls with the same
+    arguments; the call runs the attention alone."""
     p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal, q_split, q_offset2)
-    d = make_desc(p, softmax_scale, variant)
+    if kv_prebuilt and workspace is None:
+        raise ValueError("kv_prebuilt needs the workspace the rows were rebuilt into")
+    d = make_desc(p, softmax_scale, variant, FLAG_KV_PREBUILT if kv_prebuilt else 0)
     L = lib()
     dev = q.device
     if out is None:
@@ -202,6 +211,21 @@ def bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, q_offset: int = 0, causal: 
                              _ptr(out), _ptr(lse), _ptr(dout), _ptr(g["dq"]), _ptr(g["dc_kv"]), _ptr(g["dk_rope"]),
                              _ptr(g["dW_UK"]), _ptr(g["dW_UV"]), _ptr(ws), nbytes, _stream(dev)))
     return g
+
+
+def reconstruct_rows(q, c_kv, k_rope, W_UK, W_UV, row0: int, rows: int, workspace: torch.Tensor,
+                     q_offset: int = 0, causal: bool = True, q_split: int = 0, q_offset2: int = 0,
+                     variant: str = "auto"):
+    """laga_mla_reconstruct_rows: the forward's K/V rebuild for latent rows
+    [row0, row0 + rows) into `workspace` (of at least fwd_workspace_bytes), for a
+    later fwd(..., workspace=workspace, kv_prebuilt=True) with the same arguments.
+    row0 a multiple of 128; row0 + rows a multiple of 128 or past the last row any
+    query sees."""
+    p = problem_of(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal, q_split, q_offset2)
+    d = make_desc(p, None, variant)
+    nbytes = workspace.numel() * workspace.element_size()
+    _raise_if(lib().laga_mla_reconstruct_rows(ctypes.byref(d), _ptr(c_kv), _ptr(W_UK), _ptr(W_UV), int(row0),
+                                              int(rows), _ptr(workspace), nbytes, _stream(q.device)))
 
 
 def absorbed_fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset: int = 0, causal: bool = True,

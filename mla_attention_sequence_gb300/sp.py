@@ -27,6 +27,15 @@ the local op is a parameter, by default the library's C-ABI forward and
 backward (laga.fwd / laga.bwd), so the exchange logic can be exercised on CPU
 with any op of the same signature. Remote latent rows always land in this
 rank's memory through the collective before any kernel reads them.
+
+Overlapped forward (overlap=True): the gather runs as one broadcast per source
+rank, all issued asynchronously in one global order; this rank rebuilds K_nope
+and V for its own rows at once (laga.reconstruct_rows into the forward's
+workspace), then for each remote chunk waits for its broadcast and rebuilds
+its rows while the later broadcasts are still in flight; the attention then
+runs on the prebuilt K/V (laga.fwd with kv_prebuilt) and the backward reuses
+them (reuse_kv). The local steps come from an ops object (LibraryOps by
+default) so that the chunk logic also runs on CPU ranks.
 """
 from __future__ import annotations
 
@@ -81,6 +90,30 @@ class Layout:
         return torch.argsort(owner)
 
 
+class LibraryOps:
+    """The overlapped path's local steps through the library's C ABI."""
+
+    def prepare(self, q, c_kv, k_rope, W_UK, W_UV, pos, causal):
+        from . import laga
+        p = laga.problem_of(q, c_kv, k_rope, W_UK, W_UV, pos["q_offset"], causal, pos["q_split"], pos["q_offset2"])
+        return torch.empty(laga.bwd_workspace_bytes(p), dtype=torch.uint8, device=q.device)
+
+    def rebuild(self, q, c_kv, k_rope, W_UK, W_UV, pos, causal, row0, rows, ws):
+        from . import laga
+        laga.reconstruct_rows(q, c_kv, k_rope, W_UK, W_UV, row0, rows, ws, pos["q_offset"], causal, pos["q_split"],
+                              pos["q_offset2"])
+
+    def fwd_prebuilt(self, q, c_kv, k_rope, W_UK, W_UV, pos, causal, ws):
+        from . import laga
+        return laga.fwd(q, c_kv, k_rope, W_UK, W_UV, pos["q_offset"], causal, workspace=ws, q_split=pos["q_split"],
+                        q_offset2=pos["q_offset2"], kv_prebuilt=True)
+
+    def bwd_reuse(self, q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos, causal, ws):
+        from . import laga
+        return laga.bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos["q_offset"], causal, workspace=ws,
+                        reuse_kv=True, q_split=pos["q_split"], q_offset2=pos["q_offset2"])
+
+
 def _local_fwd_default(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal, q_split, q_offset2):
     from . import laga
     return laga.fwd(q, c_kv, k_rope, W_UK, W_UV, q_offset, causal, q_split=q_split, q_offset2=q_offset2)
@@ -100,12 +133,16 @@ class SPAttention:
     k_rope_shard [B, S/SP, d_rope]; and the full W_UK, W_UV (replicated)."""
 
     def __init__(self, layout: Layout, group=None, causal: bool = True,
-                 local_fwd: Callable | None = None, local_bwd: Callable | None = None):
+                 local_fwd: Callable | None = None, local_bwd: Callable | None = None,
+                 overlap: bool = False, ops=None):
         self.layout = layout
         self.group = group
         self.causal = causal
         self.local_fwd = local_fwd or _local_fwd_default
         self.local_bwd = local_bwd or _local_bwd_default
+        self.overlap = overlap
+        self.ops = ops or LibraryOps()
+        self._ws = None
         self.rank = dist.get_rank(group)
         if dist.get_world_size(group) != layout.sp:
             raise ValueError("the process group's size must equal the layout's SP degree")
@@ -144,11 +181,50 @@ class SPAttention:
         dist.all_reduce(dW_UV, op=dist.ReduceOp.SUM, group=self.group)
         return dW_UK, dW_UV
 
+    def _global_rank(self, group_rank: int) -> int:
+        return group_rank if self.group is None else dist.get_global_rank(self.group, group_rank)
+
+    def gather_and_rebuild(self, q, c_kv_shard, k_rope_shard, W_UK, W_UV, pos):
+        """The overlapped gather: returns the full c_kv, k_rope and the workspace
+        holding K_nope / V rebuilt for every row, chunk by chunk as chunks arrive."""
+        B, n, d_c = c_kv_shard.shape
+        S, sp = self.layout.seq, self.layout.sp
+        packed = torch.cat([c_kv_shard, k_rope_shard], dim=2).contiguous()
+        bufs, works = [], []
+        for src in range(sp):  # one global order on every rank
+            buf = packed if src == self.rank else torch.empty_like(packed)
+            works.append(dist.broadcast(buf, src=self._global_rank(src), group=self.group, async_op=True))
+            bufs.append(buf)
+        c_full = torch.empty((B, S, d_c), dtype=packed.dtype, device=packed.device)
+        r_full = torch.empty((B, S, packed.shape[2] - d_c), dtype=packed.dtype, device=packed.device)
+        ws = self.ops.prepare(q, c_full, r_full, W_UK, W_UV, pos, self.causal)
+        order = [self.rank] + [r for r in range(sp) if r != self.rank]  # own rows first: no wait
+        for src in order:
+            if src != self.rank:
+                works[src].wait()
+            off = 0
+            for a, length in self.layout.segments(src):  # (first row, rows)
+                b = a + length
+                c_full[:, a:b] = bufs[src][:, off:off + length, :d_c]
+                r_full[:, a:b] = bufs[src][:, off:off + length, d_c:]
+                off += length
+                # the chunk that ends the sequence also covers the padded rows past it
+                self.ops.rebuild(q, c_full, r_full, W_UK, W_UV, pos, self.causal, a, (b - a) + (127 if b == S else 0),
+                                 ws)
+        works[self.rank].wait()
+        return c_full, r_full, ws
+
     # ---------------------------------------------------------------- the block
     def forward(self, q, c_kv_shard, k_rope_shard, W_UK, W_UV):
         """Returns this rank's out [B, S/SP, n_h, d_v] and lse [B, n_h, S/SP]."""
-        c_kv, k_rope = self.gather_latent(c_kv_shard, k_rope_shard)
         pos = self.layout.query_args(self.rank)
+        if self.overlap:
+            c_kv, k_rope, ws = self.gather_and_rebuild(q, c_kv_shard, k_rope_shard, W_UK, W_UV, pos)
+            out, lse = self.ops.fwd_prebuilt(q, c_kv, k_rope, W_UK, W_UV, pos, self.causal, ws)
+            self._ws = ws
+            self._saved = (q, c_kv, k_rope, W_UK, W_UV, out, lse)
+            return out, lse
+        c_kv, k_rope = self.gather_latent(c_kv_shard, k_rope_shard)
         out, lse = self.local_fwd(q, c_kv, k_rope, W_UK, W_UV, pos["q_offset"], self.causal, pos["q_split"],
                                   pos["q_offset2"])
         self._saved = (q, c_kv, k_rope, W_UK, W_UV, out, lse)
@@ -161,8 +237,12 @@ class SPAttention:
             raise RuntimeError("backward before forward")
         q, c_kv, k_rope, W_UK, W_UV, out, lse = self._saved
         pos = self.layout.query_args(self.rank)
-        g = self.local_bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos["q_offset"], self.causal,
-                           pos["q_split"], pos["q_offset2"])
+        if self._ws is not None:  # overlapped forward: its workspace still holds K_nope / V
+            g = self.ops.bwd_reuse(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos, self.causal, self._ws)
+            self._ws = None
+        else:
+            g = self.local_bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos["q_offset"], self.causal,
+                               pos["q_split"], pos["q_offset2"])
         dc, dr = self.scatter_latent_grad(g["dc_kv"], g["dk_rope"])
         dWk, dWv = self.reduce_weight_grads(g["dW_UK"], g["dW_UV"])
         self._saved = None

@@ -98,9 +98,26 @@ def test_two_segment_shards_are_checked_before_launch(L):
 
 def test_unknown_flag_bits_rejected(L):
     d = desc()
-    d.flags = 2
+    d.flags = 4  # bits 0 (REUSE_KV) and 1 (KV_PREBUILT) are defined
     assert call_fwd(L, d) == 1
     assert b"flags" in L.laga_mla_last_error()
+
+
+def test_reconstruct_rows_argument_checks(L):
+    """laga_mla_reconstruct_rows rejects bad row ranges and unsupported paths before
+    any launch (no device memory is touched: the checks precede the workspace)."""
+    from mla_attention_sequence_gb300 import laga
+    fn = L.laga_mla_reconstruct_rows
+    fn.argtypes = [ctypes.POINTER(laga.LagaDesc), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    p16 = ctypes.c_void_p(256)  # aligned, never dereferenced: every call below fails a check first
+    d = desc(variant="materialize")
+    for row0, rows in ((64, 128), (-128, 128), (0, 0), (0, 100)):
+        assert fn(ctypes.byref(d), p16, p16, p16, row0, rows, None, 0, None) == 1, (row0, rows)
+    assert fn(ctypes.byref(d), p16, p16, p16, 0, 128, None, 0, None) == 3  # workspace missing
+    f32 = desc(dtype="f32")
+    assert fn(ctypes.byref(f32), p16, p16, p16, 0, 128, None, 0, None) == 2  # CUDA-core path: unsupported
 
 
 def test_unsupported_tensor_core_dims(L):

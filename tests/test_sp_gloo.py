@@ -77,6 +77,76 @@ def _rank_main(rank, world, port, kind, errfile):
         raise
 
 
+class _OracleOps:
+    """The overlapped path's local steps on CPU: the rebuild records each row range
+    with the latent rows it saw at that moment; the forward checks that the
+    ranges cover the sequence and runs the oracle on the gathered latent."""
+
+    def prepare(self, q, c_kv, k_rope, W_UK, W_UV, pos, causal):
+        return {"rebuilt": []}
+
+    def rebuild(self, q, c_kv, k_rope, W_UK, W_UV, pos, causal, row0, rows, ws):
+        end = min(row0 + rows, c_kv.shape[1])
+        ws["rebuilt"].append((row0, end, c_kv[:, row0:end].clone(), k_rope[:, row0:end].clone()))
+
+    def fwd_prebuilt(self, q, c_kv, k_rope, W_UK, W_UV, pos, causal, ws):
+        covered = sorted((a, e) for a, e, _, _ in ws["rebuilt"])
+        assert covered[0][0] == 0 and covered[-1][1] == c_kv.shape[1]
+        assert all(covered[k][1] == covered[k + 1][0] for k in range(len(covered) - 1)), covered
+        return _oracle_fwd(q, c_kv, k_rope, W_UK, W_UV, pos["q_offset"], causal, pos["q_split"], pos["q_offset2"])
+
+    def bwd_reuse(self, q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos, causal, ws):
+        return _oracle_bwd(q, c_kv, k_rope, W_UK, W_UV, out, lse, dout, pos["q_offset"], causal, pos["q_split"],
+                           pos["q_offset2"])
+
+
+def _rank_main_overlap(rank, world, port, kind, errfile):
+    try:
+        os.environ["MASTER_ADDR"] = "127.0.0.1"
+        os.environ["MASTER_PORT"] = str(port)
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        import oracle
+        p = PROBLEM
+        x = {k: torch.from_numpy(v.astype(np.float64)) for k, v in make_inputs(p, seed=78).items()}
+        lay = Layout(seq=p.S, sp=world, kind=kind)
+        rows = lay.rows(rank)
+        ops = _OracleOps()
+        att = SPAttention(lay, causal=True, overlap=True, ops=ops)
+        captured = {}
+        orig_prepare = ops.prepare
+
+        def prepare(*a):
+            captured["ws"] = orig_prepare(*a)
+            return captured["ws"]
+        ops.prepare = prepare
+        out, lse = att.forward(x["q"][:, rows].contiguous(), x["c_kv"][:, rows].contiguous(),
+                               x["k_rope"][:, rows].contiguous(), x["W_UK"], x["W_UV"])
+        # every chunk was rebuilt after its rows had arrived, own rows first
+        rebuilt = captured["ws"]["rebuilt"]
+        for a, e, c, r in rebuilt:
+            assert torch.equal(c, x["c_kv"][:, a:e]) and torch.equal(r, x["k_rope"][:, a:e]), (a, e)
+        own = [(a, a + n) for a, n in lay.segments(rank)]
+        assert [(a, e) for a, e, _, _ in rebuilt[:len(own)]] == own
+        g = att.backward(x["dout"][:, rows].contiguous())
+        n = {k: v.numpy() for k, v in x.items()}
+        ro, rl = oracle.mla_forward(n["q"], n["c_kv"], n["k_rope"], n["W_UK"], n["W_UV"], 0, True)
+        rg = oracle.mla_backward(n["q"], n["c_kv"], n["k_rope"], n["W_UK"], n["W_UV"], n["dout"], 0, True)
+        r = rows.numpy()
+        np.testing.assert_allclose(out.numpy(), ro[:, r], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse.numpy(), rl[:, :, r], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(g["dq"].numpy(), rg["dq"][:, r], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dc_kv"].numpy(), rg["dc_kv"][:, r], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dk_rope"].numpy(), rg["dk_rope"][:, r], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dW_UK"].numpy(), rg["dW_UK"], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(g["dW_UV"].numpy(), rg["dW_UV"], rtol=1e-10, atol=1e-12)
+        dist.barrier()
+        dist.destroy_process_group()
+    except BaseException as e:  # report to the parent, which fails the test
+        with open(f"{errfile}.{rank}", "w") as f:
+            f.write(repr(e))
+        raise
+
+
 def _free_port():
     with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
         s.bind(("127.0.0.1", 0))
@@ -117,3 +187,15 @@ def test_bytes_per_step_of_the_dsv3_layer():
     b = att.bytes_per_step(B=1, d_c=512, d_rope=64, n_h=128, d_nope=128, d_v=128)
     assert b["all_gather"] == pytest.approx(16384 * 576 * 2 * 7 / 8)
     assert b["reduce_scatter"] == b["all_gather"]
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "zigzag"])
+def test_sp_overlapped_gather_two_gloo_ranks(kind, tmp_path):
+    """The overlapped forward: per-source broadcasts, each chunk rebuilt once its
+    rows have arrived (own rows first), then the attention on the prebuilt K/V;
+    results equal the SP = 1 oracle's."""
+    errfile = str(tmp_path / "err")
+    mp.start_processes(_rank_main_overlap, args=(2, _free_port(), kind, errfile), nprocs=2, join=True,
+                       start_method="spawn")
+    for r in range(2):
+        assert not os.path.exists(f"{errfile}.{r}"), open(f"{errfile}.{r}").read()
