@@ -18,10 +18,11 @@
 // Head boundaries. A CTA pays its start (TMEM, barriers, the first tiles' load
 // latency) once for G heads. When head u's last dP^T has been issued, the MMA
 // warp releases the key/value tile (kv_empty) and the producer loads head u+1's
-// K_nope and V over it (the RoPE key stays); when head u's last dK has finished
-// (acc_done), the key-row warps move dV and dK_nope from TMEM to global memory,
-// zero the dK_nope columns and release the accumulators (acc_free) for head u+1's
-// first dV, while the tensor pipe already runs head u+1's first S^T and dP^T.
+// K_nope and V over it (the RoPE key stays). The key-row warps move dV to global
+// memory as soon as head u's last dV has finished (dv_done), while the tensor
+// pipe still runs its last dK; when that has finished (acc_done) they move
+// dK_nope, zero its columns and release the accumulators (acc_free) for head
+// u+1's first dV, while the tensor pipe already runs head u+1's first S^T and dP^T.
 //
 // Warp roles (352 threads):
 //   warp 0      lane 0: TMA for the key/value tile, then Q, dO, lse, D tiles
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* dp_free = bars + 16;   // dP^T(i) read into registers: dP(i+1) may overwrite it
   uint64_t* kv_empty = bars + 18;  // a head's last dP^T is done: the next head's K_nope, V may load
   uint64_t* acc_free = bars + 19;  // dV and dK_nope drained (and dK_nope zeroed) for the next head
+  uint64_t* dv_done = bars + 20;   // a head's last dV is done (one phase per head)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(ds_full(1), SOFTMAX_WARPS);
     mbar_init(dp_free, SOFTMAX_WARPS);
     mbar_init(acc_done, 1);
+    mbar_init(dv_done, 1);
     mbar_init(drain, 1);
     mbar_init(kv_empty, 1);
     mbar_init(acc_free, SOFTMAX_WARPS);
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma4_ts_warp(tmem + COL_DV, pt + packed_col(0), pt + packed_col(1), pt + packed_col(2),
                        pt + packed_col(3), do_mn, do_mn + (2048 >> 4), do_mn + (4096 >> 4), do_mn + (6144 >> 4),
                        IDESC_DV, i > 0 ? 1u : 0u);
+          if (i + 1 == n_qt) mma_commit_warp(dv_done);  // head u's dV is final
           if (i + 1 < n_qt) {
             if (!ready()) { ok = false; break; }  // dP^T(i) read out: dP(i+1) may overwrite it
             issue_dp(gs + 1);
@@ -398,7 +402,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (!ok) break;
-      if (n_qt <= 0) mma_commit_warp(kv_empty);  // no MMA read the tile
+      if (n_qt <= 0) {  // no MMA read the tile or wrote the accumulators
+        mma_commit_warp(kv_empty);
+        mma_commit_warp(dv_done);
+      }
       mma_commit_warp(acc_done);  // head u's accumulators are final
     }
 #ifdef LAGA_TRACE
@@ -440,13 +447,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // with the next head's tiles): warpgroup `half` moves dV and dK_nope columns
     // [64*half, 64*half + 64) of its 32 rows as bf16 (dK scaled by the softmax
     // scale) and, after the group's last head, the RoPE-key columns [32*half,
-    // 32*half + 32) (fp32, this head group's partial). After each head's steps its
-    // accumulators are moved out, dK_nope is zeroed and both are released
-    // (acc_free) for the next head's first dV and dK, while the tensor pipe runs
-    // the next head's first S^T and dP^T. A 32-column chunk of the warp's 32 rows
-    // goes TMEM -> registers -> the warp's scratch (row-per-thread) -> global
-    // memory as 4 stores of 8 rows x 64 contiguous bytes (row-per-thread global
-    // stores touch 32 lines per instruction and made a drain ~6K cycles long).
+    // 32*half + 32) (fp32, this head group's partial). dV leaves once the head's
+    // last dV has finished, while its last dK still runs; dK_nope once that has
+    // finished, after which its columns are zeroed and both accumulators are
+    // released (acc_free) for the next head's first dV and dK, while the tensor
+    // pipe runs the next head's first S^T and dP^T. Both 32-column chunks of an
+    // accumulator are loaded from TMEM together (one load latency per
+    // accumulator); each chunk of the warp's 32 rows then goes registers -> the
+    // warp's scratch (row-per-thread) -> global memory as 4 stores of 8 rows x 64
+    // contiguous bytes (row-per-thread global stores touch 32 lines per
+    // instruction and made a drain ~6K cycles long).
     uint8_t* scr = smem + OFF_SCR + (warp - 2) * SCR_BYTES;
     const long long row0 = static_cast<long long>(b) * p.skv_pad + kv0 + quarter * 32;  // the warp's first row
     auto put_chunk = [&](const uint32_t (&w)[16], auto&& dst_of_row) {
@@ -463,21 +473,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     };
     const bool z = n_qt <= 0;  // no query sees this key tile: the accumulators were never written
-    auto drain = [&](int hh, bool is_dk) {  // head hh's dV (or dK_nope) columns of this warpgroup
-#pragma unroll 1
+    // this warpgroup's two 32-column chunks of dV (or dK_nope), both loads in flight
+    auto drain_load = [&](bool is_dk, uint32_t (&a)[32], uint32_t (&c)[32]) {
+      const uint32_t col = tmem + lane_off + (is_dk ? COL_DK : COL_DV) + 64 * half;
+      tmem_ld32(col, a);
+      tmem_ld32(col + 32, c);
+    };
+    // head hh's two loaded chunks, as bf16, to global memory
+    auto drain_put = [&](int hh, bool is_dk, const uint32_t (&a)[32], const uint32_t (&c)[32]) {
+      const float sc = is_dk ? p.scale : 1.f;
+      bf16* base = is_dk ? p.dk_ws : p.dv_ws;
+#pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int c = 2 * half + j;
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + (is_dk ? COL_DK : COL_DV) + 32 * c, v);
-        tmem_wait_ld();
-        const float sc = is_dk ? p.scale : 1.f;
+        const uint32_t(&v)[32] = j ? c : a;
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           w[k] = z ? 0u : pack_bf16x2(__uint_as_float(v[2 * k]) * sc, __uint_as_float(v[2 * k + 1]) * sc);
-        bf16* base = is_dk ? p.dk_ws : p.dv_ws;
+        const int col = 64 * half + 32 * j;
         put_chunk(w, [&](long long row) {
-          return reinterpret_cast<uint8_t*>(base + (row * p.n_h + hh) * 128 + 32 * c);
+          return reinterpret_cast<uint8_t*>(base + (row * p.n_h + hh) * 128 + col);
         });
       }
     };
@@ -566,22 +581,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(ds_full(gs));
         if (lane == 0) LAGA_TRACE_POINT(dkdv, 13, gs);
       }
-      if (!ok || !warp_wait(acc_done, u & 1, 64)) { ok = false; break; }
+      if (!ok || !warp_wait(dv_done, u & 1, 65)) { ok = false; break; }
+      tc_fence_after();
+      {
+        uint32_t a[32], c[32];
+        drain_load(false, a, c);
+        tmem_wait_ld();
+        drain_put(h, false, a, c);
+      }
+      if (!warp_wait(acc_done, u & 1, 64)) { ok = false; break; }
       if (lane == 0) LAGA_TRACE_POINT(dkdv, 29, u);
       tc_fence_after();
-      drain(h, false);
-      drain(h, true);
-      if (lane == 0) LAGA_TRACE_POINT(dkdv, 27, u);
-      if (u + 1 < G) {
-        // dK_nope restarts from zero for the next head (its first dK accumulates)
-        uint32_t zero[32];
+      {
+        uint32_t a[32], c[32];
+        drain_load(true, a, c);
+        tmem_wait_ld();
+        if (u + 1 < G) {
+          // dK_nope restarts from zero for the next head (its first dK accumulates);
+          // its values are in registers, so the accumulators can be released first
+          uint32_t zero[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) zero[k] = 0u;
-        tmem_st32(tmem + lane_off + COL_DK + 32 * (2 * half), zero);
-        tmem_st32(tmem + lane_off + COL_DK + 32 * (2 * half + 1), zero);
-        tmem_wait_st();
-        release(acc_free);
-      } else {
+          for (int k = 0; k < 32; ++k) zero[k] = 0u;
+          tmem_st32(tmem + lane_off + COL_DK + 64 * half, zero);
+          tmem_st32(tmem + lane_off + COL_DK + 64 * half + 32, zero);
+          tmem_wait_st();
+          release(acc_free);
+        }
+        drain_put(h, true, a, c);
+      }
+      if (lane == 0) LAGA_TRACE_POINT(dkdv, 27, u);
+      if (u + 1 == G) {
         // the RoPE-key gradient summed over this group's heads: fp32 partial hg,
         // columns [32*half, 32*half + 32) as two 16-column (64-byte) chunks
         uint32_t v[32];
