@@ -70,8 +70,8 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + K_BYTES;
 constexpr int OFF_STAGE = OFF_V + V_BYTES;
 constexpr int OFF_ROWV = OFF_STAGE + NSTAGE * STAGE_BYTES;
-// per key-row warp, a [32 rows][64 B] scratch (64-byte swizzle) through which the
-// accumulator drain turns row-per-thread data into coalesced global stores
+// per key-row warp, a [32 rows][64 B] scratch (64-byte swizzle, 512-byte aligned)
+// from which the accumulator drain's tensor-map stores read
 constexpr int SCR_BYTES = 32 * 64;
 constexpr int OFF_SCR = OFF_ROWV + NSTAGE * 2 * ROWV_BYTES;
 constexpr int OFF_BARS = OFF_SCR + 8 * SCR_BYTES;
@@ -102,15 +102,14 @@ struct Params {
   float scale, scale_log2;
   const float* lse2;
   const float* delta;
-  bf16* dk_ws;
-  bf16* dv_ws;
-  float* dkr_ws;
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                          const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
-                         const __grid_constant__ CUtensorMap mdO, const Params p) {
+                         const __grid_constant__ CUtensorMap mdO, const __grid_constant__ CUtensorMap mdK,
+                         const __grid_constant__ CUtensorMap mdV, const __grid_constant__ CUtensorMap mdKR,
+                         const Params p) {
   extern __shared__ uint8_t smem_raw[];
   LAGA_TRACE_CTA_BEGIN(dkdv);
   LAGA_TRACE_POINT(dkdv, 30, 0);
@@ -453,23 +452,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // released (acc_free) for the next head's first dV and dK, while the tensor
     // pipe runs the next head's first S^T and dP^T. Both 32-column chunks of an
     // accumulator are loaded from TMEM together (one load latency per
-    // accumulator); each chunk of the warp's 32 rows then goes registers -> the
-    // warp's scratch (row-per-thread) -> global memory as 4 stores of 8 rows x 64
-    // contiguous bytes (row-per-thread global stores touch 32 lines per
-    // instruction and made a drain ~6K cycles long).
+    // accumulator); each chunk of the warp's 32 rows (64 bytes a row) then goes
+    // registers -> the warp's scratch -> one tensor-map store, which the TMA unit
+    // carries out while the warp goes on. (Global stores issued by the warp itself
+    // held up its next shared-memory accesses, barrier waits included, until the
+    // drain's 32 KB per warpgroup had left the SM: ~1K cycles before the next
+    // head's first P^T could start.)
     uint8_t* scr = smem + OFF_SCR + (warp - 2) * SCR_BYTES;
-    const long long row0 = static_cast<long long>(b) * p.skv_pad + kv0 + quarter * 32;  // the warp's first row
-    auto put_chunk = [&](const uint32_t (&w)[16], auto&& dst_of_row) {
-      __syncwarp();  // the previous chunk's scratch reads are done
+    const int row0 = b * p.skv_pad + kv0 + quarter * 32;  // the warp's first row
+    auto put_chunk = [&](const uint32_t (&w)[16], const CUtensorMap* map, int x) {
+      if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the scratch
+      __syncwarp();
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
         *reinterpret_cast<uint4*>(scr + sw64_offset(lane, q4)) = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+      fence_proxy_async_smem();
       __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int rr = 8 * k + (lane >> 2), ch = lane & 3;
-        *reinterpret_cast<uint4*>(dst_of_row(row0 + rr) + 16 * ch) =
-            *reinterpret_cast<const uint4*>(scr + sw64_offset(rr, ch));
+      if (lane == 0) {
+        tma_store_2d(map, scr, x, row0);
+        bulk_commit_group();
       }
     };
     const bool z = n_qt <= 0;  // no query sees this key tile: the accumulators were never written
@@ -482,7 +483,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // head hh's two loaded chunks, as bf16, to global memory
     auto drain_put = [&](int hh, bool is_dk, const uint32_t (&a)[32], const uint32_t (&c)[32]) {
       const float sc = is_dk ? p.scale : 1.f;
-      bf16* base = is_dk ? p.dk_ws : p.dv_ws;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint32_t(&v)[32] = j ? c : a;
@@ -490,10 +490,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           w[k] = z ? 0u : pack_bf16x2(__uint_as_float(v[2 * k]) * sc, __uint_as_float(v[2 * k + 1]) * sc);
-        const int col = 64 * half + 32 * j;
-        put_chunk(w, [&](long long row) {
-          return reinterpret_cast<uint8_t*>(base + (row * p.n_h + hh) * 128 + col);
-        });
+        put_chunk(w, is_dk ? &mdK : &mdV, hh * 128 + 64 * half + 32 * j);
       }
     };
     auto release = [&](uint64_t* bar) {
@@ -621,12 +618,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           uint32_t w[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) w[k] = z ? 0u : __float_as_uint(__uint_as_float(v[16 * hh + k]) * p.scale);
-          put_chunk(w, [&](long long row) {
-            return reinterpret_cast<uint8_t*>(p.dkr_ws + (row * p.n_hg + hg) * 64 + 32 * half + 16 * hh);
-          });
+          put_chunk(w, &mdKR, hg * 64 + 32 * half + 16 * hh);
         }
       }
     }
+    if (lane == 0) bulk_wait_read_all();  // shared memory must not go away under a store
   }
 
   LAGA_TRACE_POINT(dkdv, 28, 0);
@@ -680,6 +676,29 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
     r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  // the drain's stores: [32 rows][64 bytes] boxes, 64-byte swizzle, of dK_nope and dV
+  // ([B * skv_pad rows][n_h * 128] bf16) and of the RoPE-key partials
+  // ([B * skv_pad rows][n_h / G * 64] fp32)
+  CUtensorMap mdK, mdV, mdKR;
+  const int G = dkdv_heads_per_cta(d.n_h);
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t dims[2] = {kv_inner, kv_rows};
+    const uint64_t strides[1] = {kv_inner * 2};
+    const uint32_t box[2] = {32, 32};
+    r.cu = make_tmap(&mdK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.dk_ws, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
+    if (r.cu == CUDA_SUCCESS)
+      r.cu = make_tmap(&mdV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.dv_ws, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
+  }
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h / G) * 64;
+    const uint64_t dims[2] = {inner, kv_rows};
+    const uint64_t strides[1] = {inner * 4};
+    const uint32_t box[2] = {16, 32};
+    r.cu = make_tmap(&mdKR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w.dkr_ws, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
+  }
   if (r.cu != CUDA_SUCCESS) {
     r.what = "tensor maps attention backward (dK, dV)";
     return r;
@@ -699,18 +718,15 @@ LaunchResult tc_attn_bwd_dkdv(const Dims& d, const bf16* q, const bf16* k_rope, 
   p.scale_log2 = d.scale * 1.4426950408889634f;
   p.lse2 = w.lse2;
   p.delta = w.delta;
-  p.dk_ws = w.dk_ws;
-  p.dv_ws = w.dv_ws;
-  p.dkr_ws = w.dkr_ws;
-  p.G = dkdv_heads_per_cta(d.n_h);
-  p.n_hg = d.n_h / p.G;
+  p.G = G;
+  p.n_hg = d.n_h / G;
   p.successor = sm_count();
   r.err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (r.err != cudaSuccess) {
     r.what = "cudaFuncSetAttribute(attn_bwd_dkdv)";
     return r;
   }
-  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, p.n_hg, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, p);
+  attn_bwd_dkdv_kernel<<<dim3(d.skv_pad / BKV, p.n_hg, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdO, mdK, mdV, mdKR, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_bwd_dkdv_kernel launch";
   return r;

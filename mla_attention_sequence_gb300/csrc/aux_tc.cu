@@ -8,7 +8,14 @@
 
 namespace laga {
 
-bool tc_supported(const Dims& d) { return d.d_c == 512 && d.d_nope == 128 && d.d_v == 128 && d.d_rope == 64; }
+// The fixed head dims of the tensor-core kernels; their tensor-map row coordinates
+// (batch * padded rows) are 32-bit.
+bool tc_supported(const Dims& d) {
+  const int64_t rows_lim = int64_t(1) << 31;
+  return d.d_c == 512 && d.d_nope == 128 && d.d_v == 128 && d.d_rope == 64 &&
+         static_cast<int64_t>(d.B) * d.skv_pad < rows_lim && static_cast<int64_t>(d.B) * d.sq_pad < rows_lim &&
+         static_cast<int64_t>(d.B) * d.S < rows_lim;
+}
 
 int dkdv_heads_per_cta(int n_h) { return n_h % 4 == 0 ? 4 : (n_h % 2 == 0 ? 2 : 1); }
 
