@@ -47,6 +47,7 @@ constexpr int K_BYTES = 3 * BOX;
 constexpr int V_BYTES = 2 * BOX;
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_BYTES;
+static_assert(8 * 6144 <= Q_BYTES, "the epilogue stages 8 warps x 6 KB in the Q tile's space");
 constexpr int OFF_V = OFF_K + K_STAGES * K_BYTES;
 constexpr int OFF_BARS = OFF_V + V_STAGES * V_BYTES;
 constexpr int SMEM_BYTES = OFF_BARS + 256 + 1024;
@@ -67,7 +68,6 @@ struct Params {
   const float* lse2;
   const float* delta;
   const bf16* dout;  // [B][Sq][n_h][128]
-  bf16* dq;
 };
 
 // TMEM column of packed bf16 chunk k (16 keys) of dS(j): warpgroup g packs its
@@ -89,7 +89,7 @@ __device__ __forceinline__ int n_kv_tiles(const Params& p, int t) {
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                        const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap mdQ, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   LAGA_TRACE_CTA_BEGIN(dq);
   LAGA_TRACE_POINT(dq, 30, 0);
@@ -370,26 +370,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && warp_wait(dq_done, 0, 82)) {
       LAGA_TRACE_POINT(dq, 29, 0);
       tc_fence_after();
-      const bool valid = q_row < p.Sq;
-      bf16* dst = p.dq + ((static_cast<long long>(b) * p.Sq + q_row) * p.n_h + h) * 192;
+      // Epilogue: dq (scaled, bf16) through shared memory and tensor-map stores,
+      // which the TMA unit carries out while the CTA ends. Every MMA has finished,
+      // so the Q tile's space is free: each warp stages its 32 rows x 96 columns
+      // as three [32 rows][64 B] boxes (64-byte swizzle); rows past Sq are clipped
+      // by the map.
+      uint8_t* stage = smem + OFF_Q + (warp - 2) * 6144;
 #pragma unroll 1
-      for (int c = 3 * half; c < 3 * half + 3; ++c) {
+      for (int j = 0; j < 3; ++j) {
+        const int c = 3 * half + j;
         uint32_t u[32];
         tmem_ld32(tmem + COL_DQ + lane_off + c * 32, u);  // warp-collective: every lane takes part
         tmem_wait_ld();
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        uint8_t* box = stage + j * 2048;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * p.scale, __uint_as_float(u[8 * v + 1]) * p.scale);
-            o.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * p.scale, __uint_as_float(u[8 * v + 3]) * p.scale);
-            o.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * p.scale, __uint_as_float(u[8 * v + 5]) * p.scale);
-            o.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * p.scale, __uint_as_float(u[8 * v + 7]) * p.scale);
-            d4[v] = o;
-          }
+        for (int v = 0; v < 4; ++v) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * p.scale, __uint_as_float(u[8 * v + 1]) * p.scale);
+          o.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * p.scale, __uint_as_float(u[8 * v + 3]) * p.scale);
+          o.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * p.scale, __uint_as_float(u[8 * v + 5]) * p.scale);
+          o.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * p.scale, __uint_as_float(u[8 * v + 7]) * p.scale);
+          *reinterpret_cast<uint4*>(box + sw64_offset(lane, v)) = o;
         }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) tma_store_3d(&mdQ, stage + j * 2048, h * 192 + 32 * (3 * half + j), t * BQ + quarter * 32, b);
+        bulk_commit_group();
+        bulk_wait_read_all();  // shared memory must not go away under a store
+      }
+      __syncwarp();
     }
   }
 
@@ -437,6 +449,14 @@ LaunchResult tc_attn_bwd_dq(const Dims& d, const bf16* q, const bf16* k_rope, co
     r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  CUtensorMap mdQ;  // dq's [32 rows][32] boxes, 3D over [B][Sq][n_h*192]: rows past Sq clip
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 192;
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
+    const uint32_t box[3] = {32, 32, 1};
+    r.cu = make_tmap(&mdQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dq, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+  }
   if (r.cu != CUDA_SUCCESS) {
     r.what = "tensor maps attention backward (dq)";
     return r;
@@ -458,13 +478,12 @@ LaunchResult tc_attn_bwd_dq(const Dims& d, const bf16* q, const bf16* k_rope, co
   p.lse2 = w.lse2;
   p.delta = w.delta;
   p.dout = dout;
-  p.dq = dq;
   r.err = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (r.err != cudaSuccess) {
     r.what = "cudaFuncSetAttribute(attn_bwd_dq)";
     return r;
   }
-  attn_bwd_dq_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, p);
+  attn_bwd_dq_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mdQ, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_bwd_dq_kernel launch";
   return r;

@@ -45,6 +45,7 @@ constexpr int NBUF = 3;  // S/P buffers in TMEM
 constexpr int PREFETCH = 4;
 constexpr int SMEM_BYTES = Q_BYTES + K_STAGES * K_BYTES + V_STAGES * V_BYTES + 1024 + 256;
 constexpr int NTHREADS = 256;
+static_assert(4 * 8192 <= Q_BYTES, "the epilogue stages 4 warps x 8 KB in the Q tile's space");
 constexpr int WAITER_WARP = 7;
 constexpr int HANDOFF_BAR = 1;  // named barrier of warp 1 and the waiter (64 threads)
 constexpr uint32_t TMEM_COLS = 512;
@@ -62,7 +63,6 @@ struct FwdParams {
   int Sq, S, n_h, q_offset, causal, skv_pad, n_q_tiles;
   int q_split, q_offset2;  // second query segment (q_split = 0: none)
   float scale_log2;  // softmax scale * log2(e), > 0
-  bf16* out;
   float* lse;
 };
 
@@ -80,7 +80,7 @@ __device__ __forceinline__ int n_kv_tiles(const FwdParams& p, int t) {
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mR, const __grid_constant__ CUtensorMap mV,
-                    const FwdParams p) {
+                    const __grid_constant__ CUtensorMap mO, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   LAGA_TRACE_CTA_BEGIN(fwd);
   LAGA_TRACE_POINT(fwd, 30, 0);
@@ -404,29 +404,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && warp_wait(&pv_done[(n_kv - 1) % NBUF], ((n_kv - 1) / NBUF) & 1, 19)) {
       LAGA_TRACE_POINT(fwd, 29, 0);
       tc_fence_after();
+      // Epilogue: O / l as bf16 through shared memory and tensor-map stores, which
+      // the TMA unit carries out while the CTA ends (row-per-thread global stores
+      // touch 32 lines per instruction and keep the warp busy until they have left
+      // the SM). Every MMA has finished, so the Q tile's space is free: each warp
+      // stages its 32 rows as two [32 rows][128 B] boxes (128-byte swizzle, the
+      // 16-byte chunk k of row r at r * 128 + ((k ^ (r & 7)) << 4)); rows past Sq
+      // are clipped by the map.
       const uint32_t o_addr = tmem + COL_O + lane_off;
-      const bool valid = q_row < p.Sq;
       const float inv = 1.f / l_run;
-      bf16* orow = p.out + ((static_cast<long long>(b) * p.Sq + q_row) * p.n_h + h) * 128;
+      uint8_t* stage = sQ + quarter * 8192;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
         tmem_ld32(o_addr + c * 32, u);
         tmem_wait_ld();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        uint8_t* box = stage + (c >> 1) * 4096 + lane * 128;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
-            dst[v] = w;
-          }
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
+          const uint32_t k = static_cast<uint32_t>((c & 1) * 4 + v);
+          *reinterpret_cast<uint4*>(box + ((k ^ (lane & 7u)) << 4)) = w;
         }
       }
-      if (valid)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&mO, stage, h * 128, t * BQ + quarter * 32, b);
+        tma_store_3d(&mO, stage + 4096, h * 128 + 64, t * BQ + quarter * 32, b);
+        bulk_commit_group();
+        bulk_wait_read_all();  // shared memory must not go away under a store
+      }
+      __syncwarp();
+      if (q_row < p.Sq)
         p.lse[(static_cast<long long>(b) * p.n_h + h) * p.Sq + q_row] =
             (m_run + __log2f(l_run)) * 0.6931471805599453f;
     }
@@ -476,6 +490,14 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
     r.cu = make_tmap(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k_rope, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  CUtensorMap mO;  // the output's [32 rows][64] boxes, 3D over [B][Sq][n_h*128]: rows past Sq clip
+  if (r.cu == CUDA_SUCCESS) {
+    const uint64_t inner = static_cast<uint64_t>(d.n_h) * 128;
+    const uint64_t dims[3] = {inner, static_cast<uint64_t>(d.Sq), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {inner * 2, inner * 2 * d.Sq};
+    const uint32_t box[3] = {64, 32, 1};
+    r.cu = make_tmap(&mO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (r.cu != CUDA_SUCCESS) {
     r.what = "tensor maps attention forward";
     return r;
@@ -491,7 +513,6 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
   p.skv_pad = d.skv_pad;
   p.n_q_tiles = (d.Sq + BQ - 1) / BQ;
   p.scale_log2 = d.scale * LOG2E;
-  p.out = out;
   p.lse = lse;
   p.status = device_status_ptr();
   r.err = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -499,7 +520,7 @@ LaunchResult tc_attn_fwd(const Dims& d, const bf16* q, const bf16* k_ws, const b
     r.what = "cudaFuncSetAttribute(attn_fwd)";
     return r;
   }
-  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, p);
+  attn_fwd_kernel<<<dim3(p.n_q_tiles, d.n_h, d.B), NTHREADS, SMEM_BYTES, st>>>(mQ, mK, mR, mV, mO, p);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) r.what = "attn_fwd_kernel launch";
   return r;
