@@ -56,14 +56,14 @@ def load_peaks():
 # DRAM traffic per launch of a kernel, from one ncu capture of the kernel source
 # identified by `src_sha` (sha256 of the kernel file followed by csrc/ptx.cuh,
 # first 16 hex digits). It is reported only while the source is unchanged.
-# attn_bwd_dkdv: dram__bytes_read.sum + dram__bytes_write.sum = 740.7 + 563.0 MB
+# attn_bwd_dkdv: dram__bytes_read.sum + dram__bytes_write.sum = 741.1 + 563.5 MB
 # on the n_h = 64 last-rank shard (the full n_h = 128 shard exceeds the size rule
 # for a multi-pass capture); the kernel's work and both byte streams (K/V and
 # Q/dO tiles in, dK/dV and the head-group RoPE-key partials out) scale with the
 # head count, so x2.
 MEASURED_TRAFFIC = {
-    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "ee553712b728cd19",
-                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (740.726528e6 + 563.041536e6)}},
+    "attn_bwd_dkdv": {"src": "attn_bwd_dkdv_tc.cu", "src_sha": "bfc25970d5f2b0f6",
+                      "bytes_per_launch": {"dsv3_sp8_rank7_S16384_h128": 2 * (741.058304e6 + 563.450880e6)}},
 }
 
 
@@ -422,6 +422,9 @@ def run_ours(args, name: str):
     # interference (compute slower) from dependency stalls (gaps between steps)
     c_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     c_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # and each step's copies on their streams, to tell slow host copies (a step
+    # waiting for its inputs) from a host thread that enqueues too late
+    cp_ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] for k in ("h0", "h1", "o0", "o1")}
     barrier(world)
     torch.cuda.synchronize()
     e_start.record(stream)
@@ -433,8 +436,10 @@ def run_ours(args, name: str):
         if i >= 2:
             copy_in.wait_event(done[b])  # step i-2 has finished reading this set's inputs
         with torch.cuda.stream(copy_in):
+            cp_ev["h0"][i].record(copy_in)
             for key, (hv, _) in shared.items():
                 dev_in[key].copy_(hv, non_blocking=True)
+            cp_ev["h1"][i].record(copy_in)
             in_ready[b].record(copy_in)
         stream.wait_event(in_ready[b])
         if i >= 2:
@@ -446,11 +451,13 @@ def run_ours(args, name: str):
         done[b].record(stream)
         copy_out.wait_event(done[b])
         with torch.cuda.stream(copy_out):
+            cp_ev["o0"][i].record(copy_out)
             for buf, oh in zip(sbufs, outs_host):
                 oh["out"].copy_(buf.out, non_blocking=True)
                 oh["lse"].copy_(buf.lse, non_blocking=True)
                 for k, v in buf.grads.items():
                     oh[k].copy_(v, non_blocking=True)
+            cp_ev["o1"][i].record(copy_out)
             out_done[b].record(copy_out)
     stream.wait_stream(copy_out)
     e_end.record(stream)
@@ -459,6 +466,10 @@ def run_ours(args, name: str):
     laga.check(dev)
     e2e_ms = reduce_max(e_start.elapsed_time(e_end), world, dev)
     e2e_compute_ms = float(np.mean([a.elapsed_time(z) for a, z in zip(c_start, c_end)]))
+    e2e_gap_ms = float(np.mean([c_end[i].elapsed_time(c_start[i + 1]) for i in range(args.steps - 1)])) \
+        if args.steps > 1 else 0.0
+    e2e_h2d_ms = float(np.mean([a.elapsed_time(z) for a, z in zip(cp_ev["h0"], cp_ev["h1"])]))
+    e2e_d2h_ms = float(np.mean([a.elapsed_time(z) for a, z in zip(cp_ev["o0"], cp_ev["o1"])]))
 
     flops = sum(p.flops_step() for p in problems)
     tokens = sum(p.B * p.Sq for p in problems)
@@ -522,7 +533,8 @@ def run_ours(args, name: str):
             "kernels_ms_per_launch": kernel_ms,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "compute_ms_per_step": e2e_compute_ms,
-                    "ms_per_step": e2e_ms / args.steps},
+                    "gap_ms_between_steps": e2e_gap_ms, "h2d_ms_per_step": e2e_h2d_ms,
+                    "d2h_ms_per_step": e2e_d2h_ms, "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": gpu_launches,
             "clocks": clk,
             "cpu_baseline": cpu,
