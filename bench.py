@@ -527,6 +527,9 @@ def run_ours(args, name: str):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": cfg,
             "tokens_per_s": tokens_s,
+            # secondary: FlashAttention convention (adds the backward's score recompute)
+            "tflops_fa_convention": world * sum(p.flops_step_fa() for p in problems) * args.steps
+            / (total_ms * 1e-3) / 1e12,
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "peak_source": peaks["source"],
             "roofline": roof,

@@ -72,6 +72,11 @@ class Problem:
     def flops_step(self) -> int:
         return self.flops_fwd() + self.flops_bwd()
 
+    def flops_step_fa(self) -> int:
+        """The step under the FlashAttention convention: the algorithmic flops plus
+        the backward's recomputation of the scores, 2 * pairs * n_h * d_qk."""
+        return self.flops_step() + 2 * self.pairs * self.n_h * self.d_qk
+
     def with_(self, **kw) -> "Problem":
         return replace(self, **kw)
 

@@ -116,3 +116,18 @@ def test_oracle_sample_weight_gradients_sum_over_the_batch():
         np.testing.assert_allclose(k["dq_h"], g["dq"][0, :, h], rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(k["out_h"], out[0, :, h], rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(k["lse_h"], lse[0, h], rtol=1e-12, atol=1e-14)
+
+
+def test_flop_conventions_at_the_dsv3_shard():
+    """The algorithmic step count and the FlashAttention convention at the DSV3 SP=8
+    last-rank shard, against the closed forms: 2048 queries at offset 14336 see
+    2048 * 14336 + 2048 * 2049 / 2 = 31,458,304 keys in all; the step is three times
+    the forward (attention 2 * P * n_h * 320, reconstruction 2 * 16384 * 512 * n_h * 256),
+    and the FlashAttention convention adds the backward's score recompute 2 * P * n_h * 192."""
+    from mla_attention_sequence_gb300.configs import dsv3_rank
+    p = dsv3_rank(7)
+    P = 2048 * 14336 + 2048 * 2049 // 2
+    assert p.pairs == P == 31_458_304
+    fwd = 2 * P * 128 * 320 + 2 * 16384 * 512 * 128 * 256
+    assert p.flops_step() == 3 * fwd
+    assert p.flops_step_fa() - p.flops_step() == 2 * P * 128 * 192
