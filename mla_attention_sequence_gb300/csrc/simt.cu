@@ -348,7 +348,8 @@ LaunchResult bwd_t(const Dims& d, const T* q, const T* c_kv, const T* k_rope, co
   kq<<<dim3(d.Sq, d.n_h, d.B), 128, smem_q, st>>>(d, q, w.kn, w.v, k_rope, dout, lse, w.delta, dq);
   kk<<<dim3(d.S, d.n_h, d.B), 128, smem_k, st>>>(d, q, w.kn, w.v, k_rope, dout, lse, w.delta, w.dkn, w.dkr, w.dv);
   const ll nr = static_cast<ll>(d.B) * d.S * d.d_rope;
-  simt_sum_heads<T><<<static_cast<unsigned>((nr + 255) / 256), 256, 0, st>>>(d, w.dkr, dk_rope);
+  if (nr > 0)  // no RoPE part (d_rope = 0): no RoPE-key gradient to sum
+    simt_sum_heads<T><<<static_cast<unsigned>((nr + 255) / 256), 256, 0, st>>>(d, w.dkr, dk_rope);
   r.err = cudaGetLastError();
   if (r.err != cudaSuccess) {
     r.what = "simt attention backward";

@@ -72,3 +72,38 @@ def test_random_shape_matches_oracle(built, c):
     p, scale = draw_case(c)
     x = make_inputs(p, seed=500 + c)
     assert_close(run_gpu(p, x, scale=scale), run_oracle(p, x, scale=scale), TOL["bf16"], tag=f"case {c}: {p}")
+
+
+N_SIMT = 16
+
+
+def draw_simt_case(c: int):
+    """Case c of the fp32 draw for the CUDA-core path (any widths): random head
+    widths, d_rope = 0 included, at the fp32 tolerance (1e-4 * max|oracle|)."""
+    from mla_attention_sequence_gb300.configs import Problem
+    rng = np.random.default_rng(7000 + c)
+    d_c = int(rng.choice([16, 24, 64]))
+    d_nope = int(rng.choice([8, 16, 32]))
+    d_rope = int(rng.choice([0, 4, 16]))
+    d_v = int(rng.choice([8, 12, 32]))
+    B, n_h = int(rng.integers(1, 3)), int(rng.integers(1, 5))
+    causal = bool(rng.random() < 0.75)
+    S = int(rng.integers(1, 60))
+    Sq = int(rng.integers(1, S + 1)) if causal else int(rng.integers(1, 40))
+    q_offset = int(rng.integers(0, S - Sq + 1)) if causal else 0
+    return Problem(B=B, Sq=Sq, S=S, n_h=n_h, d_c=d_c, d_nope=d_nope, d_rope=d_rope, d_v=d_v, q_offset=q_offset,
+                   causal=causal, dtype="f32")
+
+
+def test_simt_draw_spans_zero_rope_and_both_masks():
+    ps = [draw_simt_case(c) for c in range(N_SIMT)]
+    assert any(p.d_rope == 0 for p in ps) and any(p.d_rope > 0 for p in ps)
+    assert {p.causal for p in ps} == {True, False}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", range(N_SIMT))
+def test_random_simt_shape_matches_oracle(built, c):
+    p = draw_simt_case(c)
+    x = make_inputs(p, seed=800 + c)
+    assert_close(run_gpu(p, x), run_oracle(p, x), TOL["f32"], tag=f"simt case {c}: {p}")
