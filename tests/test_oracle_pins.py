@@ -609,3 +609,95 @@ def test_head_parallel_oracle_helper_matches_the_oracle():
     ref.update(out=out, lse=lse)
     for k, r in ref.items():
         np.testing.assert_allclose(got[k], r, rtol=1e-12, atol=1e-14, err_msg=k)
+
+
+# --------------------------------------------------------------------------- random tiny shapes
+def draw_tiny(c):
+    """Seeded random tiny problem c (fp64 inputs): batch, heads and every width drawn,
+    d_rope = 0 included; causal or not; one or two query segments; the default or an
+    explicit scale."""
+    rng = np.random.default_rng(4000 + c)
+    d_rope = int(rng.choice([0, 1, 3]))
+    causal = bool(rng.random() < 0.7)
+    S = int(rng.integers(2, 12))
+    two = bool(rng.random() < 0.4) and S >= 3
+    if two:
+        n0, n1 = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+        Sq = n0 + n1
+        off0 = int(rng.integers(0, S - n0 + 1)) if causal else 0
+        off1 = int(rng.integers(0, S - n1 + 1)) if causal else 0
+        seg = dict(q_split=n0, q_offset2=off1)
+    else:
+        Sq = int(rng.integers(1, S + 1)) if causal else int(rng.integers(1, 6))
+        off0 = int(rng.integers(0, S - Sq + 1)) if causal else 0
+        seg = {}
+    p = Problem(B=int(rng.integers(1, 3)), Sq=Sq, S=S, n_h=int(rng.integers(1, 4)), d_c=int(rng.integers(1, 6)),
+                d_nope=int(rng.integers(1, 5)), d_rope=d_rope, d_v=int(rng.integers(1, 5)), q_offset=off0,
+                causal=causal, dtype="f32", **seg)
+    scale = float(rng.uniform(0.2, 1.5)) if rng.random() < 0.5 else None
+    return p, scale
+
+
+def positions(p):
+    """Absolute position of each local query row: rows [0, q_split) at q_offset + i,
+    rows [q_split, Sq) at q_offset2 + (i - q_split)."""
+    return [p.q_offset + i if (p.q_split == 0 or i < p.q_split) else p.q_offset2 + i - p.q_split
+            for i in range(p.Sq)]
+
+
+def brute_force_forward_at(p, x, scale, pos):
+    """brute_force_forward with each query row at an explicit position."""
+    out = np.zeros((p.B, p.Sq, p.n_h, p.d_v))
+    lse = np.zeros((p.B, p.n_h, p.Sq))
+    for b in range(p.B):
+        for h in range(p.n_h):
+            K = [[sum(x["c_kv"][b, j, c] * x["W_UK"][c, h * p.d_nope + d] for c in range(p.d_c))
+                  for d in range(p.d_nope)] + [x["k_rope"][b, j, d] for d in range(p.d_rope)] for j in range(p.S)]
+            V = [[sum(x["c_kv"][b, j, c] * x["W_UV"][c, h * p.d_v + d] for c in range(p.d_c)) for d in range(p.d_v)]
+                 for j in range(p.S)]
+            for i in range(p.Sq):
+                keys = range(0, (pos[i] if p.causal else p.S - 1) + 1)
+                s = {j: scale * sum(x["q"][b, i, h, d] * K[j][d] for d in range(p.d_qk)) for j in keys}
+                m = max(s.values())
+                z = sum(math.exp(s[j] - m) for j in keys)
+                lse[b, h, i] = m + math.log(z)
+                for d in range(p.d_v):
+                    out[b, i, h, d] = sum(math.exp(s[j] - m) / z * V[j][d] for j in keys)
+    return out, lse
+
+
+@pytest.mark.parametrize("c", range(12))
+def test_random_tiny_shapes_brute_force_and_finite_differences(c):
+    """The oracle's forward against the scalar-loop brute force, and its backward
+    against central differences of <dout, out> along random directions, on random
+    tiny shapes (two-segment shards and d_rope = 0 among them)."""
+    p, scale = draw_tiny(c)
+    x = inputs64(p, seed=300 + c)
+    sc = scale if scale is not None else 1.0 / math.sqrt(p.d_nope + p.d_rope)
+    out, lse = oracle.mla_forward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], p.q_offset, p.causal, scale,
+                                  p.q_split, p.q_offset2)
+    out_bf, lse_bf = brute_force_forward_at(p, x, sc, positions(p))
+    np.testing.assert_allclose(out, out_bf, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_bf, rtol=1e-11, atol=1e-12)
+
+    def f(xx):
+        o, _ = oracle.mla_forward(xx["q"], xx["c_kv"], xx["k_rope"], xx["W_UK"], xx["W_UV"], p.q_offset, p.causal,
+                                  scale, p.q_split, p.q_offset2)
+        return float((o * xx["dout"]).sum())
+
+    g = oracle.mla_backward(x["q"], x["c_kv"], x["k_rope"], x["W_UK"], x["W_UV"], x["dout"], p.q_offset, p.causal,
+                            scale, p.q_split, p.q_offset2)
+    grads = {"q": g["dq"], "c_kv": g["dc_kv"], "k_rope": g["dk_rope"], "W_UK": g["dW_UK"], "W_UV": g["dW_UV"]}
+    rng = np.random.default_rng(50 + c)
+    h = 1e-6
+    for name, grad in grads.items():
+        assert grad.shape == x[name].shape, name
+        if grad.size == 0:
+            continue
+        direction = rng.standard_normal(x[name].shape)
+        xp, xm = dict(x), dict(x)
+        xp[name] = x[name] + h * direction
+        xm[name] = x[name] - h * direction
+        fd = (f(xp) - f(xm)) / (2 * h)
+        an = float((grad * direction).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (c, name, fd, an)
